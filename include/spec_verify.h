@@ -1,0 +1,163 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched speculative-sampling
+ * verify step.
+ *
+ * The operation.  For each of B sequences with K_b drafted tokens x_0..x_{K_b-1}
+ * (0 <= K_b <= K_max), the target gives logits at K_b + 1 positions and the
+ * draft gives a distribution at K_b positions over one shared vocabulary of V
+ * tokens.  The step:
+ *   1. applies temperature, then top-k, then top-p to every target row and to
+ *      every draft row given as logits, and softmaxes each row
+ *      ("NOTE-159: Accelerating Large Language Model Decoding with Speculative
+ *      Sampling", Key results: sampling knobs applied to the probabilities
+ *      before the rejection step; Recommendations R3);
+ *   2. walks the drafts left to right and accepts x_j iff u_j < p_t(x_j) /
+ *      p_d(x_j), stopping at the first rejection j*
+ *      ("Accelerating Large Language Model Decoding with Speculative Sampling",
+ *      The algorithm; "57 Speculative Decoding", the listing "One speculative
+ *      decoding loop");
+ *   3. resamples position j* from max(0, p_t - p_d) renormalised, by inverse CDF
+ *      in ascending token id, or, when every draft passed, samples one bonus
+ *      token from the target row at position K_b + 1
+ *      ("Speculative Decoding from Scratch", The big picture (2.1) step 3 and
+ *      The heart of it (2.3); "Speculative Decoding: Getting 3x Speedups
+ *      Without Changing the Model", How It Works, steps 3-4).
+ * The output of a sequence is x_0..x_{j*-1} followed by the sampled token:
+ * between 1 and K_b + 1 tokens.
+ *
+ * Uniforms.  Philox4x32-10 (Salmon et al., SC'11) keyed by the 64-bit seed;
+ * counter = ((j << 2) | tag, b, round_lo, round_hi); u = (word >> 8) * 2^-24.
+ * Tag 0: word 0 is the accept uniform of slot j, word 1 the sampling uniform
+ * of slot j (the resample at j*, or the bonus at j = K_b).  Tag 1, word 0:
+ * the uniform of the draft-side sampler for slot j.
+ *
+ * Conventions.
+ *  - Every tensor pointer is DEVICE memory owned by the caller, contiguous,
+ *    row-major.  The library never frees or keeps caller memory.
+ *  - A handle owns only its device workspace, sized at create time for
+ *    max_batch x max_k x vocab.  One handle must not run on two streams at
+ *    once; create one handle per concurrent stream.
+ *  - spec_verify_run and spec_draft_sample are asynchronous on the given
+ *    stream (a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream): no host synchronisation and no allocation.
+ *  - Errors found on the host return a status and launch nothing.  Data
+ *    errors found on the device are reported per sequence in row_status (see
+ *    SPEC_ROW_*); such sequences get tokens = -1 and num_accepted = -1.
+ *  - -inf logits are allowed (masked tokens, probability 0).  A NaN or +inf
+ *    logit, or a row with no finite logit, in any row the step reads makes
+ *    the sequence SPEC_ROW_NONFINITE.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spec_verify* spec_verify_t; /* opaque handle */
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* a NULL required pointer, a size out of range, a bad knob */
+    SPEC_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement          */
+    SPEC_ERR_OOM = 3,         /* workspace allocation failed (create only)              */
+    SPEC_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed            */
+    SPEC_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait ran out           */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+typedef enum { SPEC_TARGET_LOGITS = 0, SPEC_TARGET_HIDDEN_LMHEAD = 1 } spec_target_kind;
+typedef enum { SPEC_DRAFT_LOGITS = 0, SPEC_DRAFT_PROBS = 1 } spec_draft_kind;
+
+/* per-sequence row_status values */
+enum {
+    SPEC_ROW_OK = 0,
+    SPEC_ROW_BAD_TOKEN = 1,     /* a drafted token at j < K_b outside [0, V)              */
+    SPEC_ROW_BAD_K = 2,         /* K_b outside [0, K_max]                                 */
+    SPEC_ROW_NONFINITE = 3,     /* NaN / +inf / no finite logit; or a negative, NaN or    */
+                                /* +inf draft probability where one is read               */
+    SPEC_ROW_ZERO_RESIDUAL = 4  /* the residual summed to 0 after a rejection (rounding   */
+                                /* only): the token was drawn from p_t; output is valid   */
+};
+
+typedef struct {
+    int32_t device;       /* CUDA device ordinal                                     */
+    int32_t max_batch;    /* largest B of any run                                    */
+    int32_t max_k;        /* largest K_max of any run                                */
+    int32_t vocab;        /* V (>= 1), shared by target and draft                    */
+    int32_t hidden;       /* H of the fused LM head (SPEC_TARGET_HIDDEN_LMHEAD), else 0 */
+    int32_t target_kind;  /* spec_target_kind                                        */
+    int32_t target_dtype; /* spec_dtype of the target logits                         */
+    int32_t draft_kind;   /* spec_draft_kind                                         */
+    int32_t draft_dtype;  /* logits: equal to target_dtype; probabilities: SPEC_F32  */
+} spec_verify_config;
+
+typedef struct {
+    float temperature; /* T > 0.  T == 0 (greedy) returns SPEC_ERR_UNSUPPORTED       */
+    int32_t top_k;     /* 0 or >= V: off; else keep the k highest logits, ties to   */
+                       /* the lower token id                                         */
+    float top_p;       /* >= 1: off; in (0, 1): keep the rank-ordered prefix whose   */
+                       /* mass strictly before each kept token is < top_p            */
+    int32_t reserved;  /* must be 0                                                  */
+    uint64_t seed;     /* Philox key                                                 */
+    uint64_t round;    /* Philox counter words 2-3 (one value per verify round)      */
+} spec_sampling;
+
+typedef struct {
+    const void* target;          /* [B, k_max+1, V] logits of target_dtype; or, for the */
+                                 /* LM head, hidden states [B*(k_max+1), H] bf16        */
+    const void* w_vocab;         /* [H, V] bf16 for the LM head, else NULL              */
+    const void* draft;           /* [B, k_max, V]: logits (draft_dtype) or f32 probs    */
+    const int32_t* draft_tokens; /* [B, k_max]; slots j >= K_b are ignored              */
+    const int32_t* k_per_row;    /* [B] per-sequence K_b, or NULL for K_b = k_max       */
+    int32_t batch;               /* B, 0 <= B <= max_batch (0 is a no-op)               */
+    int32_t k_max;               /* padded draft length of this run, <= max_k           */
+} spec_verify_inputs;
+
+typedef struct {
+    int32_t* tokens;        /* [B, k_max+1] emitted tokens, -1 padded (required)      */
+    int32_t* num_accepted;  /* [B] accepted drafts j* (required); emitted = j* + 1     */
+    int32_t* row_status;    /* [B] SPEC_ROW_* or NULL                                 */
+    float* p_t_at_draft;    /* [B, k_max] p_t(x_j) after knobs, NaN for j >= K_b; or NULL */
+    float* p_d_at_draft;    /* [B, k_max] p_d(x_j), NaN for j >= K_b; or NULL          */
+    float* residual_mass;   /* [B] sum of max(0, p_t - p_d) at j*, 0 if all accepted; or NULL */
+    float* target_lse;      /* [B, k_max+1] log-sum-exp of l/T over the kept set, NaN  */
+                            /* beyond K_b; or NULL                                     */
+} spec_verify_outputs;
+
+/* Allocate a handle and its device workspace on cfg->device.
+ * Returns SPEC_ERR_INVALID_ARG for sizes < 1 (max_k may be 0) or a dtype/kind
+ * combination outside the table above, SPEC_ERR_UNSUPPORTED for the LM-head
+ * target kind when this build lacks it, SPEC_ERR_OOM when the workspace does
+ * not fit.  On error *out is NULL. */
+spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out);
+
+/* One verify step for a batch (the operation described at the top).  All
+ * outputs are written on `stream`; the call returns before they are ready. */
+spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in,
+                            const spec_sampling* s, const spec_verify_outputs* out,
+                            void* stream);
+
+/* Draft-side sampler, the step before the verify: x = sample(q) of the listing
+ * "One speculative decoding loop" ("57 Speculative Decoding").  For every
+ * sequence b and slot j < K_b: draws draft_tokens[b, j] ~ P_d[b, j] (the draft
+ * row after the knobs when it is logits, as given when it is probabilities) by
+ * inverse CDF with the tag-1 uniform; slots j >= K_b get -1.  When draft_probs
+ * is not NULL it receives the dense post-knob draft distribution [B, k_max, V]
+ * (f32; rows j >= K_b untouched).  `draft` has the handle's draft kind/dtype. */
+spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t* k_per_row,
+                              int32_t batch, int32_t k_max, const spec_sampling* s,
+                              int32_t* draft_tokens, float* draft_probs, void* stream);
+
+/* Free the handle and its workspace (synchronises its device first). */
+spec_status spec_verify_destroy(spec_verify_t h);
+
+/* Static English text for a status code. */
+const char* spec_verify_status_string(spec_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,307 @@
+// sv_api.cu -- the C ABI (include/spec_verify.h): argument checks, workspace,
+// launch sequence.  Host code only; every step of the computation runs in the
+// kernels of sv_rows.cu and sv_sample.cu.
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "sv_internal.cuh"
+#include "spec_verify.h"
+
+using namespace sv;
+
+struct spec_verify {
+    spec_verify_config cfg;
+    int64_t rows_cap;     // max_batch * (2 * max_k + 1)
+    int64_t jobs_cap;     // max_batch * max(1, max_k)
+    int nseg_cap, nchunk_cap, nseg_sample;
+    void* ws;
+    size_t ws_bytes;
+    SegStat* seg;
+    uint16_t* chunk;
+    RowStat* rstat;
+    int32_t* kept_id;
+    float* kept_l;
+    unsigned* row_ticket;
+    unsigned* seq_ticket;
+    Job* jobs;
+    unsigned long long* job_seg;
+    unsigned* job_ticket;
+};
+
+namespace {
+
+int elem_size(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+int seg_elems(int dtype) { return SEG_BYTES / elem_size(dtype); }
+int chunk_elems(int dtype) { return CHUNK_BYTES / elem_size(dtype); }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// knobs of one launch; SPEC_OK or the error to return
+spec_status fill_knobs(const spec_verify* h, const spec_sampling* s, Params& p)
+{
+    if (!s || s->reserved != 0) return SPEC_ERR_INVALID_ARG;
+    const float T = s->temperature;
+    if (!(T >= 0.f) || isinf(T)) return SPEC_ERR_INVALID_ARG;
+    if (T == 0.f) return SPEC_ERR_UNSUPPORTED;  // greedy verify is a separate mode
+    if (s->top_k < 0) return SPEC_ERR_INVALID_ARG;
+    if (!(s->top_p > 0.f)) return SPEC_ERR_INVALID_ARG;  // also rejects NaN
+    const int V = h->cfg.vocab;
+    p.T = T;
+    p.c = (float)(1.4426950408889634 / (double)T);
+    p.top_k = (s->top_k > 0 && s->top_k < V) ? s->top_k : 0;
+    p.top_p = s->top_p < 1.f ? s->top_p : 1.f;
+    p.top_p_fix = s->top_p < 1.f ? (uint64_t)((double)s->top_p * 72057594037927936.0) : 0;
+    p.seed = s->seed;
+    p.round = s->round;
+    return SPEC_OK;
+}
+
+void fill_workspace(const spec_verify* h, Params& p)
+{
+    p.seg = h->seg;
+    p.chunk = h->chunk;
+    p.rstat = h->rstat;
+    p.kept_id = h->kept_id;
+    p.kept_l = h->kept_l;
+    p.row_ticket = h->row_ticket;
+    p.seq_ticket = h->seq_ticket;
+    p.jobs = h->jobs;
+    p.job_seg = h->job_seg;
+    p.job_ticket = h->job_ticket;
+    p.nseg_sample = h->nseg_sample;
+}
+
+// the per-row merge keeps the kept set as an explicit list whenever top-k
+// bounds it by KCAP; otherwise some target rows may need the stage-2 sampler
+bool all_lists(const Params& p) { return p.top_k > 0 && p.top_k <= KCAP; }
+
+void choose_seg_mode(Params& p, int dtype)
+{
+    p.nseg = (int)cdiv(p.V, seg_elems(dtype));
+    p.nchunk = (int)cdiv(p.V, chunk_elems(dtype));
+    const bool fast = p.top_k > 0 && p.top_k <= KCAP && p.top_k <= p.nchunk &&
+                      p.nchunk <= MAX_CHUNKS;
+    p.seg_mode = fast ? SEG_CHUNK : SEG_SUM;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_verify_status_string(spec_status s)
+{
+    switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported request";
+    case SPEC_ERR_OOM: return "out of device memory";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out)
+{
+    if (!out) return SPEC_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!cfg) return SPEC_ERR_INVALID_ARG;
+    if (cfg->max_batch < 1 || cfg->max_k < 0 || cfg->vocab < 1 || cfg->device < 0)
+        return SPEC_ERR_INVALID_ARG;
+    if (cfg->target_dtype != SPEC_F32 && cfg->target_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (cfg->draft_kind == SPEC_DRAFT_LOGITS) {
+        if (cfg->draft_dtype != cfg->target_dtype) return SPEC_ERR_INVALID_ARG;
+    } else if (cfg->draft_kind == SPEC_DRAFT_PROBS) {
+        if (cfg->draft_dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+    } else {
+        return SPEC_ERR_INVALID_ARG;
+    }
+    if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD) return SPEC_ERR_UNSUPPORTED;
+    if (cfg->target_kind != SPEC_TARGET_LOGITS) return SPEC_ERR_INVALID_ARG;
+    // the stage-2 sampler scans at most NT segments per row
+    if ((int64_t)cfg->vocab > (int64_t)NT * SAMPLE_SEG) return SPEC_ERR_UNSUPPORTED;
+    if ((int64_t)cfg->max_batch * (2 * (int64_t)cfg->max_k + 1) > (int64_t)INT32_MAX / 4)
+        return SPEC_ERR_INVALID_ARG;
+
+    DeviceGuard g(cfg->device);
+    if (!g.ok) return SPEC_ERR_CUDA;
+
+    spec_verify* h = new (std::nothrow) spec_verify();
+    if (!h) return SPEC_ERR_OOM;
+    h->cfg = *cfg;
+    const int64_t V = cfg->vocab;
+    h->rows_cap = (int64_t)cfg->max_batch * (2 * (int64_t)cfg->max_k + 1);
+    h->jobs_cap = (int64_t)cfg->max_batch * (cfg->max_k > 0 ? cfg->max_k : 1);
+    int dts[2] = {cfg->target_dtype, cfg->draft_dtype};
+    h->nseg_cap = 1;
+    h->nchunk_cap = 1;
+    for (int dt : dts) {
+        h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, seg_elems(dt)));
+        h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
+    }
+    h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
+
+    // one allocation, 256-byte aligned sub-buffers
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) & ~(size_t)255;
+        return at;
+    };
+    const size_t o_seg = take(sizeof(SegStat) * h->rows_cap * h->nseg_cap);
+    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->nchunk_cap);
+    const size_t o_rstat = take(sizeof(RowStat) * h->rows_cap);
+    const size_t o_kid = take(sizeof(int32_t) * h->rows_cap * KCAP);
+    const size_t o_kl = take(sizeof(float) * h->rows_cap * KCAP);
+    const size_t o_rt = take(sizeof(unsigned) * h->rows_cap);
+    const size_t o_st = take(sizeof(unsigned) * cfg->max_batch);
+    const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
+    const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
+    const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
+    h->ws_bytes = off;
+    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return SPEC_ERR_OOM;
+    }
+    if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return SPEC_ERR_CUDA;
+    }
+    char* b = (char*)h->ws;
+    h->seg = (SegStat*)(b + o_seg);
+    h->chunk = (uint16_t*)(b + o_chunk);
+    h->rstat = (RowStat*)(b + o_rstat);
+    h->kept_id = (int32_t*)(b + o_kid);
+    h->kept_l = (float*)(b + o_kl);
+    h->row_ticket = (unsigned*)(b + o_rt);
+    h->seq_ticket = (unsigned*)(b + o_st);
+    h->jobs = (Job*)(b + o_jobs);
+    h->job_seg = (unsigned long long*)(b + o_jseg);
+    h->job_ticket = (unsigned*)(b + o_jt);
+    *out = h;
+    return SPEC_OK;
+}
+
+spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const spec_sampling* s,
+                            const spec_verify_outputs* out, void* stream)
+{
+    if (!h || !in || !s || !out) return SPEC_ERR_INVALID_ARG;
+    const spec_verify_config& cfg = h->cfg;
+    if (in->batch < 0 || in->batch > cfg.max_batch || in->k_max < 0 || in->k_max > cfg.max_k)
+        return SPEC_ERR_INVALID_ARG;
+    Params p;
+    memset(&p, 0, sizeof p);
+    spec_status st = fill_knobs(h, s, p);
+    if (st != SPEC_OK) return st;
+    if (in->batch == 0) return SPEC_OK;
+    if (!in->target || !in->draft || !out->tokens || !out->num_accepted) return SPEC_ERR_INVALID_ARG;
+    if (in->k_max > 0 && !in->draft_tokens) return SPEC_ERR_INVALID_ARG;
+
+    p.B = in->batch;
+    p.Kmax = in->k_max;
+    p.V = cfg.vocab;
+    p.rps = 2 * in->k_max + 1;
+    p.draft_launch = 0;
+    p.draft_kind = cfg.draft_kind;
+    p.target = in->target;
+    p.draft = in->draft;
+    p.xin = in->draft_tokens;
+    p.kpr = in->k_per_row;
+    p.tokens = out->tokens;
+    p.num_accepted = out->num_accepted;
+    p.row_status = out->row_status;
+    p.p_t_at = out->p_t_at_draft;
+    p.p_d_at = out->p_d_at_draft;
+    p.resid_mass = out->residual_mass;
+    p.lse = out->target_lse;
+    p.probs_out = nullptr;
+    fill_workspace(h, p);
+    const int dtype = cfg.target_dtype;
+    choose_seg_mode(p, dtype);
+    const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(in->target) &&
+                     (cfg.draft_kind == SPEC_DRAFT_PROBS || aligned16(in->draft));
+
+    DeviceGuard g(cfg.device);
+    if (!g.ok) return SPEC_ERR_CUDA;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (launch_rows(p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (!all_lists(p) && launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t* k_per_row,
+                              int32_t batch, int32_t k_max, const spec_sampling* s,
+                              int32_t* draft_tokens, float* draft_probs, void* stream)
+{
+    if (!h || !s) return SPEC_ERR_INVALID_ARG;
+    const spec_verify_config& cfg = h->cfg;
+    if (batch < 0 || batch > cfg.max_batch || k_max < 0 || k_max > cfg.max_k)
+        return SPEC_ERR_INVALID_ARG;
+    if (cfg.draft_kind != SPEC_DRAFT_LOGITS) return SPEC_ERR_UNSUPPORTED;
+    Params p;
+    memset(&p, 0, sizeof p);
+    spec_status st = fill_knobs(h, s, p);
+    if (st != SPEC_OK) return st;
+    if (batch == 0 || k_max == 0) return SPEC_OK;
+    if (!draft || !draft_tokens) return SPEC_ERR_INVALID_ARG;
+    p.B = batch;
+    p.Kmax = k_max;
+    p.V = cfg.vocab;
+    p.rps = k_max;
+    p.draft_launch = 1;
+    p.draft_kind = 0;
+    p.target = nullptr;
+    p.draft = draft;
+    p.kpr = k_per_row;
+    p.tokens = draft_tokens;
+    p.probs_out = draft_probs;
+    fill_workspace(h, p);
+    const int dtype = cfg.draft_dtype;
+    choose_seg_mode(p, dtype);
+    const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(draft);
+
+    DeviceGuard g(cfg.device);
+    if (!g.ok) return SPEC_ERR_CUDA;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (launch_rows(p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (!all_lists(p) && launch_sample(p, dtype, p.B * p.Kmax, cs) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (draft_probs && launch_probs(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+spec_status spec_verify_destroy(spec_verify_t h)
+{
+    if (!h) return SPEC_ERR_INVALID_ARG;
+    spec_status st = SPEC_OK;
+    {
+        DeviceGuard g(h->cfg.device);
+        if (!g.ok) st = SPEC_ERR_CUDA;
+        if (h->ws && cudaFree(h->ws) != cudaSuccess) st = SPEC_ERR_CUDA;
+    }
+    delete h;
+    return st;
+}
+
+}  // extern "C"
