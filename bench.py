@@ -1,0 +1,396 @@
+"""Benchmark of the batched speculative-sampling verify step on GB300.
+
+One step = one ``spec_verify_run`` over one batch (every stage of the verify
+path), on inputs already resident in HBM.  Default workload: B = 64 sequences,
+K = 8 drafts, V = 128256, bf16 logits, temperature 0.7, top-k 50 on both
+distributions.  The metric is verify rows/s (rows = sum_b (K_b + 1)) with the
+achieved HBM bandwidth of the dominant kernel against the measured peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, same workload
+
+Multi-GPU (torchrun, one rank per GPU): every rank verifies its own batch
+(weak scaling, no collective on the data path); a barrier brackets the timed
+region and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify rows/s (B·(K+1)) and achieved HBM GB/s vs GB300 peak, speculative sampling"
+UNIT = "rows/s"
+ROTATE = 3  # input copies cycled between steps (3 x 279 MB > L2)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def _workload(n: int):
+    from workloads import make_config
+    return make_config(n)
+
+
+def _wl_config(w, n_rot):
+    return {
+        "workload": w.name, "config_id": None, "B": w.B, "K": w.K_max, "V": w.V,
+        "input_dtype": w.dtype, "temperature": w.temperature, "top_k": w.top_k,
+        "top_p": w.top_p, "rows_per_step": w.rows(), "logit_bytes_per_step": w.logit_bytes(),
+        "l2": f"{n_rot} rotating input copies ({n_rot * w.logit_bytes() / 1e6:.0f} MB) > L2",
+        "parallelism": "replicas (one batch per GPU)",
+    }
+
+
+# --------------------------------------------------------------------------- #
+# clocks sampled during the timed region                                      #
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 0.5 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(busy), "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------------------- #
+# CPU baseline: the fp64 oracle as it stands, on a bounded sample             #
+# --------------------------------------------------------------------------- #
+def cpu_baseline(w, toks, seconds_target: float = 15.0, max_seq: int | None = None):
+    import oracle
+    dk = oracle.DRAFT_PROBS if w.draft_kind == "probs" else oracle.DRAFT_LOGITS
+    t0 = time.perf_counter()
+    rows = 0
+    nseq = 0
+    while True:
+        b = nseq % w.B
+        oracle.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
+                      temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed,
+                      round=w.round, b_begin=b, b_end=b + 1)
+        rows += int(w.k_per_row[b]) + 1
+        nseq += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or (max_seq and nseq >= max_seq):
+            break
+    return {"value": rows / el, "unit": UNIT, "cores": oracle.cores_used(), "kind": "oracle",
+            "sample": f"{nseq} sequences ({rows} verify rows) of the same workload, "
+                      f"{el:.1f} s single-threaded fp64",
+            "host": _host()}
+
+
+def _host():
+    try:
+        model = ""
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        return f"{os.cpu_count()} cores {model}".strip()
+    except OSError:
+        return f"{os.cpu_count()} cores"
+
+
+# --------------------------------------------------------------------------- #
+# the reference arm: the oracle on the host cores                             #
+# --------------------------------------------------------------------------- #
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    w = _workload(args.config)
+    dk = oracle.DRAFT_PROBS if w.draft_kind == "probs" else oracle.DRAFT_LOGITS
+    toks, _ = oracle.draft_sample(w.draft, w.k_per_row, draft_kind=dk,
+                                  temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                                  seed=w.seed, round=w.round)
+    per_step = max(1, args.ref_seq)
+    for i in range(args.warmup):
+        b = i % w.B
+        oracle.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
+                      temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed,
+                      b_begin=b, b_end=b + 1)
+        if i >= 2:
+            break
+    t0 = time.perf_counter()
+    rows = 0
+    for s in range(args.steps):
+        for q in range(per_step):
+            b = (s * per_step + q) % w.B
+            oracle.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
+                          temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                          seed=w.seed, b_begin=b, b_end=b + 1)
+            rows += int(w.k_per_row[b]) + 1
+    el = time.perf_counter() - t0
+    value = rows / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _wl_config(w, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.cores_used(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} sequence(s) per step of the same workload",
+                         "host": _host()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    line["config"]["l2"] = "n/a: host memory"
+    line["config"]["note"] = ("reference arm: the fp64 CPU oracle (this project's checker) on "
+                              "the host cores; the pages ship no implementation")
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# the GB300 arm                                                               #
+# --------------------------------------------------------------------------- #
+def run_gpu(args):
+    import torch
+    import speculative_decoding_verification_42_gb300 as sv
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    sv.load_library()
+    w = _workload(args.config)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    target = [to_dev(w.target)]
+    draft = [to_dev(w.draft)]
+    for _ in range(ROTATE - 1):
+        target.append(target[0].clone())
+        draft.append(draft[0].clone())
+    kpr = torch.from_numpy(w.k_per_row).to(dev)
+    ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype=w.dtype, device=local,
+                      draft_kind=w.draft_kind)
+    knobs = dict(temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed)
+    # drafted tokens: the library's draft-side sampler (tag-1 uniforms)
+    toks = ver.draft_sample(draft[0], kpr, **knobs)
+    torch.cuda.synchronize()
+    out = None
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, o):
+        c = i % ROTATE
+        return ver.run(target[c], draft[c], toks, kpr, out=o, debug=False, **knobs)
+
+    out = step(0, None)
+    for i in range(max(3, args.warmup)):
+        step(i, out)
+    torch.cuda.synchronize()
+
+    launches_per_step = 1 if (0 < w.top_k <= 1024) else 2
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    try:
+        gpu_sel = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_sel = str(local)
+    sampler = ClockSampler(gpu_sel) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step(i, out)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_launch_ms = sum(launch_ms) / K
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    rows = w.rows()
+    value = rows * K * world / (total_ms / 1e3)
+    bytes_step = w.logit_bytes()
+    peak, peak_src = _peaks()
+    achieved = bytes_step / (mean_launch_ms / 1e3) / 1e9
+
+    # end to end: host buffers through the same call, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        h_target = torch.empty(target[0].shape, dtype=target[0].dtype, pin_memory=True)
+        h_draft = torch.empty(draft[0].shape, dtype=draft[0].dtype, pin_memory=True)
+        h_target.copy_(target[0])
+        h_draft.copy_(draft[0])
+        h_toks = toks.cpu().pin_memory()
+        h_kpr = kpr.cpu().pin_memory()
+        h_out_t = torch.empty(out["tokens"].shape, dtype=torch.int32, pin_memory=True)
+        h_out_n = torch.empty(out["num_accepted"].shape, dtype=torch.int32, pin_memory=True)
+        d_toks = torch.empty_like(toks)
+        d_kpr = torch.empty_like(kpr)
+
+        def e2e_step(i):
+            c = i % ROTATE
+            target[c].copy_(h_target, non_blocking=True)
+            draft[c].copy_(h_draft, non_blocking=True)
+            d_toks.copy_(h_toks, non_blocking=True)
+            d_kpr.copy_(h_kpr, non_blocking=True)
+            o = ver.run(target[c], draft[c], d_toks, d_kpr, out=out, debug=False, **knobs)
+            h_out_t.copy_(o["tokens"], non_blocking=True)
+            h_out_n.copy_(o["num_accepted"], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if dist:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = (h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
+               + h_toks.numel() * 4 + h_kpr.numel() * 4)
+        d2h = h_out_t.numel() * 4 + h_out_n.numel() * 4
+        e2e = {"value": rows * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, toks.cpu().numpy(), seconds_target=args.cpu_seconds)
+    cfg = _wl_config(w, ROTATE)
+    cfg["config_id"] = args.config
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "hbm", "kernel": "k_rows (stage 1)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_step,
+                     "mean_launch_us": mean_launch_ms * 1e3},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    ver.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seq", type=int, default=1,
+                    help="reference arm: sequences verified by the oracle per step")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
