@@ -51,7 +51,8 @@ class _VerifyOut(C.Structure):
                 ("p_d_at_draft", C.c_void_p), ("residual_mass", C.c_void_p),
                 ("target_lse", C.c_void_p), ("alpha", C.c_void_p),
                 ("margin_accept", C.c_void_p), ("margin_topp", C.c_void_p),
-                ("margin_cdf", C.c_void_p), ("cdf_lo", C.c_void_p), ("cdf_hi", C.c_void_p)]
+                ("margin_cdf", C.c_void_p), ("cdf_lo", C.c_void_p), ("cdf_hi", C.c_void_p),
+                ("topp_margin_t", C.c_void_p), ("topp_margin_d", C.c_void_p)]
 
 
 def lib() -> C.CDLL:
@@ -196,7 +197,8 @@ def verify(target, draft, draft_tokens, k_per_row=None, *, draft_kind=DRAFT_LOGI
         target_lse=np.full((B, K + 1), np.nan), alpha=np.full((B, K), np.nan),
         margin_accept=np.full(B, np.inf), margin_topp=np.full(B, np.inf),
         margin_cdf=np.full(B, np.inf), cdf_lo=np.full(B, -1, np.int32),
-        cdf_hi=np.full(B, -1, np.int32))
+        cdf_hi=np.full(B, -1, np.int32), topp_margin_t=np.full((B, K + 1), np.inf),
+        topp_margin_d=np.full((B, K), np.inf))
     vout = _VerifyOut(*[_ptr(out[f]) for f, _ in _VerifyOut._fields_])
     s = _Sampling(float(temperature), int(top_k), float(top_p), int(seed), int(round),
                   float(delta))

@@ -317,6 +317,8 @@ int orc_verify(const orc_verify_in* in, const orc_sampling* s, orc_verify_out* o
         for (int32_t j = 0; j <= Kmax; ++j) {
             put_i(out->tokens, (int64_t)b * (Kmax + 1) + j, -1);
             put_d(out->target_lse, (int64_t)b * (Kmax + 1) + j, NAN);
+            put_d(out->topp_margin_t, (int64_t)b * (Kmax + 1) + j, INFINITY);
+            if (j < Kmax) put_d(out->topp_margin_d, (int64_t)b * Kmax + j, INFINITY);
         }
         for (int32_t j = 0; j < Kmax; ++j) {
             put_d(out->p_t_at_draft, (int64_t)b * Kmax + j, NAN);
@@ -380,6 +382,8 @@ int orc_verify(const orc_verify_in* in, const orc_sampling* s, orc_verify_out* o
             }
             put_d(out->p_t_at_draft, drow, p);
             put_d(out->p_d_at_draft, drow, q);
+            put_d(out->topp_margin_t, trow, it.topp_margin);
+            put_d(out->topp_margin_d, drow, id.topp_margin);
             put_d(out->target_lse, trow, it.M + log(it.S));
             if (out->alpha) {
                 double a = 0.0;
@@ -412,8 +416,10 @@ int orc_verify(const orc_verify_in* in, const orc_sampling* s, orc_verify_out* o
             load_row(in->target, in->target_dtype, trow, V, lrow);
             if (orc_row_dist(lrow, V, s->temperature, s->top_k, s->top_p, Pt, &it))
                 nonfinite = 1;
-            else
+            else {
                 put_d(out->target_lse, trow, it.M + log(it.S));
+                put_d(out->topp_margin_t, trow, it.topp_margin);
+            }
         }
         if (!nonfinite && jstar >= 0 && in->draft_kind == ORC_DRAFT_PROBS &&
             !probs_row_ok(Pd_star, V))

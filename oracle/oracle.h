@@ -130,6 +130,8 @@ typedef struct {
     double* margin_cdf;            /* [B] margin of the final inverse CDF  */
     int32_t* cdf_lo;               /* [B] near-tie neighbourhood of the    */
     int32_t* cdf_hi;               /* [B]   final sampled token            */
+    double* topp_margin_t;         /* [B, K_max+1] top-p margin of each target row */
+    double* topp_margin_d;         /* [B, K_max] top-p margin of each draft row    */
 } orc_verify_out;
 
 /* Verify sequences b in [b_begin, b_end).  Any output pointer may be NULL. */

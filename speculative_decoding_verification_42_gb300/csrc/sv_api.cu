@@ -18,6 +18,8 @@ struct spec_verify {
     int64_t rows_cap;     // max_batch * (2 * max_k + 1)
     int64_t jobs_cap;     // max_batch * max(1, max_k)
     int nseg_cap, nchunk_cap, nseg_sample;
+    int chunk_stride;     // chunk keys per row slot (multiple of 8: 16-byte rows)
+    int num_sms;          // streaming kernel: two CTAs per SM
     void* ws;
     size_t ws_bytes;
     SegStat* seg;
@@ -30,6 +32,9 @@ struct spec_verify {
     Job* jobs;
     unsigned long long* job_seg;
     unsigned* job_ticket;
+    unsigned long long* grab;
+    unsigned* done;
+    unsigned* err;
 };
 
 namespace {
@@ -88,6 +93,23 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.job_seg = h->job_seg;
     p.job_ticket = h->job_ticket;
     p.nseg_sample = h->nseg_sample;
+    p.chunk_stride = h->chunk_stride;
+    p.grab = h->grab;
+    p.done = h->done;
+    p.err = h->err;
+}
+
+// stage 1: stream every row (the persistent bulk-copy kernel when every row
+// starts on a 16-byte boundary, else one CTA per segment); then merge the rows
+// (one warp per row when the knobs allow, else one CTA per row) and decide the
+// sequences, each grid a programmatic dependent launch of the one before
+cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool vec,
+                          cudaStream_t s)
+{
+    cudaError_t e = vec ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
+                        : launch_rows(p, dtype, false, s);
+    if (e != cudaSuccess) return e;
+    return warp_merge_ok(p) ? launch_merge_warp(p, dtype, s) : launch_merge(p, dtype, s);
 }
 
 // the per-row merge keeps the kept set as an explicit list whenever top-k
@@ -135,6 +157,7 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
     } else {
         return SPEC_ERR_INVALID_ARG;
     }
+    if (cfg->max_k > 255) return SPEC_ERR_UNSUPPORTED;  // a decision stages 2*K_max+1 rows
     if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD) return SPEC_ERR_UNSUPPORTED;
     if (cfg->target_kind != SPEC_TARGET_LOGITS) return SPEC_ERR_INVALID_ARG;
     // the stage-2 sampler scans at most NT segments per row
@@ -159,6 +182,17 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
         h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
     }
     h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
+    h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device) !=
+        cudaSuccess) {
+        delete h;
+        return SPEC_ERR_CUDA;
+    }
+    // stage-1 work items (row slot, segment) are counted in 32-bit ints
+    if (h->rows_cap * h->nseg_cap >= (int64_t)INT32_MAX) {
+        delete h;
+        return SPEC_ERR_INVALID_ARG;
+    }
 
     // one allocation, 256-byte aligned sub-buffers
     size_t off = 0;
@@ -168,7 +202,7 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
         return at;
     };
     const size_t o_seg = take(sizeof(SegStat) * h->rows_cap * h->nseg_cap);
-    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->nchunk_cap);
+    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->chunk_stride);
     const size_t o_rstat = take(sizeof(RowStat) * h->rows_cap);
     const size_t o_kid = take(sizeof(int32_t) * h->rows_cap * KCAP);
     const size_t o_kl = take(sizeof(float) * h->rows_cap * KCAP);
@@ -177,6 +211,9 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
     const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
     const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
     const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
+    const size_t o_grab = take(sizeof(unsigned long long));
+    const size_t o_done = take(sizeof(unsigned));
+    const size_t o_err = take(sizeof(unsigned));
     h->ws_bytes = off;
     if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -199,6 +236,9 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
     h->jobs = (Job*)(b + o_jobs);
     h->job_seg = (unsigned long long*)(b + o_jseg);
     h->job_ticket = (unsigned*)(b + o_jt);
+    h->grab = (unsigned long long*)(b + o_grab);
+    h->done = (unsigned*)(b + o_done);
+    h->err = (unsigned*)(b + o_err);
     *out = h;
     return SPEC_OK;
 }
@@ -245,7 +285,7 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
-    if (launch_rows(p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_stage1(h, p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!all_lists(p) && launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
@@ -284,7 +324,7 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
-    if (launch_rows(p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_stage1(h, p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!all_lists(p) && launch_sample(p, dtype, p.B * p.Kmax, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     if (draft_probs && launch_probs(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;

@@ -23,20 +23,26 @@
 namespace sv {
 
 constexpr int NT = 256;             // threads of every CTA
-constexpr int SEG_BYTES = 32768;    // bytes of one stage-1 segment
+constexpr int SEG_BYTES = 16384;    // bytes of one stage-1 segment
 constexpr int CHUNK_BYTES = 128;    // bytes of data behind one chunk-max key
 constexpr int KCAP = 1024;          // largest kept set stored as an explicit list
-constexpr int CAND_CAP = 2048;      // candidates of the fast top-k gather
+constexpr int CAND_CAP = 1024;      // candidates of the fast top-k gather
 constexpr int MAX_CHUNKS = 8192;    // chunk keys a row merge can hold in smem
 constexpr int DIGIT_BITS = 11;      // radix digit of the general selection
 constexpr int NBINS = 1 << DIGIT_BITS;
 constexpr int SAMPLE_SEG = 4096;    // elements of one stage-2 segment
 constexpr int SAMPLE_EPT = SAMPLE_SEG / NT;
 constexpr int WALK_EPT = 16;        // contiguous elements per thread in ordered walks
+constexpr int SCRATCH_BYTES = 32768;  // shared scratch of a row merge / sequence decision
+constexpr int NSTAGE = 4;           // ring stages of the streaming kernel
+constexpr int NS = 128;             // stream threads of the streaming kernel
+// streaming kernel layout: stream warps [0, NS), one producer warp [NS, NS + 32)
+constexpr int STREAM_THREADS = NS + 32;
+constexpr int STREAM_CTAS_PER_SM = 3;
 
 enum SegMode : int32_t { SEG_SUM = 0, SEG_CHUNK = 1 };
 enum RowMode : int32_t { MODE_ALL = 0, MODE_LIST = 1, MODE_PREFIX = 2 };
-enum : int32_t { FLAG_NONFINITE = 1 };
+enum : int32_t { FLAG_NONFINITE = 1, FLAG_BLOCK_MERGE = 2 };  // 2: the warp merge gave up
 enum : int32_t { JOB_NONE = 0, JOB_RESIDUAL = 1, JOB_ROW = 2 };
 
 // status codes (same values as the public ABI)
@@ -74,6 +80,7 @@ struct Params {
     int32_t rps;          // row slots per sequence
     int32_t nseg;         // stage-1 segments per row
     int32_t nchunk;       // chunk-max keys per row
+    int32_t chunk_stride; // chunk keys per row in the workspace (multiple of 8)
     int32_t draft_launch; // 1: the draft-side sampler (rows are draft rows only)
     int32_t draft_kind;   // 0 logits, 1 probabilities (float)
     int32_t seg_mode;     // SegMode of this launch
@@ -110,6 +117,9 @@ struct Params {
     unsigned long long* job_seg;  // [njobs, nseg_sample] fixed-point segment masses
     unsigned* job_ticket;     // [njobs]
     int32_t nseg_sample;      // stage-2 segments per row
+    unsigned long long* grab; // streaming kernel: next work item (reset by the last CTA)
+    unsigned* done;           // streaming kernel: CTAs finished
+    unsigned* err;            // bounded waits that ran out (0 = none)
 };
 
 // ------------------------------------------------------------------------- //
@@ -215,8 +225,31 @@ __device__ __forceinline__ unsigned long long cdf_target(float u, unsigned long 
 }
 
 // ------------------------------------------------------------------------- //
-// block-wide helpers (NT threads)                                           //
+// block-wide helpers over the NT "compute" threads 0..NT-1.  They synchronise  //
+// with named barrier 1 of NT threads, so a CTA may carry extra threads (the    //
+// producer warp of the streaming kernel) that never join these barriers.       //
 // ------------------------------------------------------------------------- //
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+
+// barrier of the stream warps of the streaming kernel (named barrier 2)
+__device__ __forceinline__ void ssync() { asm volatile("bar.sync 2, %0;" ::"n"(NS) : "memory"); }
+
+// reductions over a thread group of NTH threads (local index lt) whose
+// barrier is SYNC(); red holds NTH/32 values
+template <int NTH, typename SYNC>
+__device__ __forceinline__ float group_max_nan(float v, float* red, int lt, SYNC sync);
+template <int NTH, typename SYNC>
+__device__ __forceinline__ double group_sum_d(double v, double* red, int lt, SYNC sync);
+
+// block-wide OR over the compute threads; flag: a shared int
+__device__ __forceinline__ bool csync_or(bool v, int* flag)
+{
+    if (threadIdx.x == 0) *flag = 0;
+    csync();
+    if (v) *flag = 1;
+    csync();
+    return *flag != 0;
+}
 template <typename F>
 __device__ __forceinline__ float warp_reduce_f(float v, F op)
 {
@@ -232,14 +265,42 @@ __device__ __forceinline__ double warp_sum_d(double v)
     return v;
 }
 
+template <int NTH, typename SYNC>
+__device__ __forceinline__ float group_max_nan(float v, float* red, int lt, SYNC sync)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    sync();
+    if ((lt & 31) == 0) red[lt >> 5] = v;
+    sync();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < NTH / 32; ++i) r = fmax_nan(r, red[i]);
+    return r;
+}
+
+template <int NTH, typename SYNC>
+__device__ __forceinline__ double group_sum_d(double v, double* red, int lt, SYNC sync)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    sync();
+    if ((lt & 31) == 0) red[lt >> 5] = v;
+    sync();
+    double r = 0.0;
+#pragma unroll
+    for (int i = 0; i < NTH / 32; ++i) r += red[i];
+    return r;
+}
+
 // all threads get the block max (NaN-propagating); red: >= NT/32 floats
 __device__ __forceinline__ float block_max_nan(float v, float* red)
 {
     v = warp_reduce_f(v, fmax_nan);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     float r = red[0];
 #pragma unroll
     for (int i = 1; i < NT / 32; ++i) r = fmax_nan(r, red[i]);
@@ -251,9 +312,9 @@ __device__ __forceinline__ double block_sum_d(double v, double* red)
 {
     v = warp_sum_d(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     double r = 0.0;
 #pragma unroll
     for (int i = 0; i < NT / 32; ++i) r += red[i];
@@ -271,9 +332,9 @@ __device__ __forceinline__ T block_excl_scan(T v, T* red, T* total)
         T y = __shfl_up_sync(0xffffffffu, x, o);
         if (l >= o) x += y;
     }
-    __syncthreads();
+    csync();
     if (l == 31) red[w] = x;
-    __syncthreads();
+    csync();
     T before = T(0), all = T(0);
 #pragma unroll
     for (int i = 0; i < NT / 32; ++i) {
@@ -300,7 +361,7 @@ __device__ __forceinline__ void bitonic_sort_u64(unsigned long long* a, int n)
                     }
                 }
             }
-            __syncthreads();
+            csync();
         }
     }
 }
@@ -401,8 +462,66 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int n, int x)
     return lo;
 }
 
+// ------------------------------------------------------------------------- //
+// TMA bulk copies and mbarriers (sm_90+ PTX)                                 //
+// ------------------------------------------------------------------------- //
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// make initialised barriers visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// a bounded wait: false when the barrier did not flip within the limit
+constexpr uint32_t WAIT_LIMIT = 1u << 24;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// one-dimensional bulk copy global -> shared, completing on an mbarrier
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
 // launchers (defined in the .cu files)
 cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_t s);
+cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);
+cudaError_t launch_merge_warp(const Params& p, int dtype, cudaStream_t s);
+// rows whose merge the warp kernel handles: fast top-k rows, or rows without knobs
+__host__ __device__ __forceinline__ bool warp_merge_ok(const Params& p)
+{
+    return !p.draft_launch && ((p.seg_mode == SEG_CHUNK && p.top_k <= 256 && p.nchunk <= 4096) ||
+                               (p.seg_mode == SEG_SUM && p.top_k == 0 && !(p.top_p < 1.0f)));
+}
 cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s);
 cudaError_t launch_probs(const Params& p, int dtype, cudaStream_t s);
 

@@ -12,39 +12,31 @@
 // Decoding from Scratch" (The heart of it, 2.3): accept x_j iff u < p_t/p_d;
 // stop at the first rejection; resample it from max(0, p_t - p_d); when all
 // pass, one more token from the target at K_b + 1 (The big picture, 2.1).
+//
+// Two kernels run the same per-segment, per-row and per-sequence code:
+//  * k_rows_tma (rows whose start is 16-byte aligned): persistent, two CTAs per
+//    SM.  A producer warp takes work items from a global counter and streams
+//    each 32 KB segment into a 3-stage shared-memory ring with bulk (TMA)
+//    copies completing on mbarriers; eight compute warps consume the ring.
+//    A merge runs in the stage it has just consumed, while the producer keeps
+//    prefetching and the other CTA of the SM keeps streaming.
+//  * k_rows: one CTA per segment, loads straight into registers (any V).
 #include "sv_internal.cuh"
 
 namespace sv {
 
-// dynamic shared memory of k_rows
-constexpr int SM_CK = MAX_CHUNKS * 2;        // chunk keys (u16)
-constexpr int SM_CAND = CAND_CAP * 8;        // candidates (u64) / histogram (u64[NBINS])
-constexpr int SM_QUAL = CAND_CAP * 4;        // qualifying chunk ids
-constexpr int SM_HIST = 256 * 4 * 2;         // two 256-bin u32 histograms
-constexpr int ROWS_SMEM = SM_CK + SM_CAND + SM_QUAL + SM_HIST;
-static_assert(SM_CAND >= NBINS * 8, "histogram must fit the candidate region");
-
-struct Smem {
-    uint16_t* ck;
-    unsigned long long* cand;  // also the u64 histogram of the general select
-    int32_t* qual;
-    uint32_t* h0;
-    uint32_t* h1;
-};
-
-__device__ __forceinline__ Smem smem_layout(unsigned char* base)
-{
-    Smem s;
-    s.ck = (uint16_t*)base;
-    s.cand = (unsigned long long*)(base + SM_CK);
-    s.qual = (int32_t*)(base + SM_CK + SM_CAND);
-    s.h0 = (uint32_t*)(base + SM_CK + SM_CAND + SM_QUAL);
-    s.h1 = s.h0 + 256;
-    return s;
-}
+// scratch layout of a merge (SCRATCH_BYTES)
+constexpr int SC_CK = 0;                         // chunk keys, u16[MAX_CHUNKS]      (16 KB)
+constexpr int SC_CAND = MAX_CHUNKS * 2;          // candidates, u64[CAND_CAP]        (8 KB)
+constexpr int SC_QUAL = SC_CAND + CAND_CAP * 8;  // qualifying chunks, i32[CAND_CAP] (4 KB)
+constexpr int SC_HIST = SC_QUAL + CAND_CAP * 4;  // two u32[256] histograms          (2 KB)
+constexpr int SC_END = SC_HIST + 2 * 256 * 4;
+static_assert(SC_END <= SCRATCH_BYTES, "merge scratch overflows");
+static_assert(NBINS * 8 <= SCRATCH_BYTES, "radix histogram overflows the scratch");
+static_assert(2 * KCAP * 8 <= SCRATCH_BYTES, "two staged kept lists overflow the scratch");
 
 // ------------------------------------------------------------------------- //
-// per-vector arithmetic of the streaming pass (16 bytes: 8 bf16 or 4 f32)     //
+// per-vector arithmetic (16 bytes: 8 bf16 or 4 f32)                           //
 // ------------------------------------------------------------------------- //
 template <typename T> struct Vec16;
 
@@ -102,56 +94,83 @@ template <> struct Vec16<float> {
     }
 };
 
-// ------------------------------------------------------------------------- //
-// the streaming pass over one segment                                       //
-// ------------------------------------------------------------------------- //
-template <typename T, bool VEC, int MODE>
-__device__ __forceinline__ void segment_pass(const Params& p, const T* row, int seg, int r,
-                                             float* redf, double* redd)
-{
-    constexpr int VW = Vec16<T>::N;
-    constexpr int SEG = SEG_BYTES / (int)sizeof(T);
-    constexpr int ROUNDS = SEG / (NT * VW);
-    constexpr int CHUNK_EL = CHUNK_BYTES / (int)sizeof(T);
-    const int V = p.V;
-    const int64_t base = (int64_t)seg * SEG;
+template <typename T, int NTH> struct SegGeom {
+    static constexpr int VW = Vec16<T>::N;
+    static constexpr int SEG = SEG_BYTES / (int)sizeof(T);
+    static constexpr int ROUNDS = SEG / (NTH * VW);
+    static constexpr int CHUNK_EL = CHUNK_BYTES / (int)sizeof(T);
+};
 
-    uint4 v[ROUNDS];
-#pragma unroll
-    for (int i = 0; i < ROUNDS; ++i) {
-        const int64_t e0 = base + ((int64_t)i * NT + threadIdx.x) * VW;
-        if (VEC)
-            v[i] = (e0 < V) ? ld_stream16(row + e0) : Vec16<T>::neg_inf();
-        else
-            v[i] = (e0 < V) ? Vec16<T>::load_scalar(row, e0, V) : Vec16<T>::neg_inf();
+// NaN-propagating max of one lane's 16 bytes, kept packed for bf16 (two maxima
+// per instruction), and its reduction over the 8 lanes of a 128-byte chunk
+template <typename T> struct ChunkMax;
+
+template <> struct ChunkMax<__nv_bfloat16> {
+    using P = uint32_t;  // two bf16 maxima
+    static __device__ __forceinline__ uint32_t mx(uint32_t a, uint32_t b)
+    {
+        __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+        __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+        __nv_bfloat162 z = __hmax2_nan(x, y);
+        return *reinterpret_cast<uint32_t*>(&z);
     }
+    static __device__ __forceinline__ P lane(uint4 w) { return mx(mx(w.x, w.y), mx(w.z, w.w)); }
+    static __device__ __forceinline__ P shfl(P v, int o) { return mx(v, __shfl_xor_sync(0xffffffffu, v, o)); }
+    static __device__ __forceinline__ float value(P v) { return fmax_nan(bf16_lo(v), bf16_hi(v)); }
+};
 
+template <> struct ChunkMax<float> {
+    using P = float;
+    static __device__ __forceinline__ P lane(uint4 w) { return Vec16<float>::vmax(w); }
+    static __device__ __forceinline__ P shfl(P v, int o) { return fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o)); }
+    static __device__ __forceinline__ float value(P v) { return v; }
+};
+
+// ------------------------------------------------------------------------- //
+// one segment: chunk-max keys (SEG_CHUNK) or (max, sum exp) (SEG_SUM), by a   //
+// group of NTH threads (local index lt, barrier sync).  fetch(i) returns      //
+// round i's 16-byte vector of this thread (or -inf padding).                 //
+// ------------------------------------------------------------------------- //
+template <typename T, int MODE, int NTH, typename F, typename SYNC>
+__device__ __forceinline__ void segment_compute(const Params& p, F fetch, int seg, int r, int lt,
+                                                SYNC sync, float* redf, double* redd)
+{
+    using G = SegGeom<T, NTH>;
+    using CM = ChunkMax<T>;
+    const int V = p.V;
+    const int64_t base = (int64_t)seg * G::SEG;
     if (MODE == SEG_CHUNK) {
         // 8 consecutive lanes hold one 128-byte chunk: its NaN-propagating max
         // becomes a 16-bit order key (a lower bound of every key in the chunk)
+        typename CM::P m[G::ROUNDS];
 #pragma unroll
-        for (int i = 0; i < ROUNDS; ++i) {
-            float m = Vec16<T>::vmax(v[i]);
-            m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            const int64_t e0 = base + ((int64_t)i * NT + threadIdx.x) * VW;
-            const int64_t ci = e0 / CHUNK_EL;
-            if ((threadIdx.x & 7) == 0 && e0 < V)
-                p.chunk[(int64_t)r * p.nchunk + ci] = (uint16_t)(key_of(m) >> 16);
+        for (int i = 0; i < G::ROUNDS; ++i) m[i] = CM::lane(fetch(i));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+            for (int i = 0; i < G::ROUNDS; ++i) m[i] = CM::shfl(m[i], o);
+        }
+        if ((lt & 7) == 0) {
+#pragma unroll
+            for (int i = 0; i < G::ROUNDS; ++i) {
+                const int64_t e0 = base + ((int64_t)i * NTH + lt) * G::VW;
+                if (e0 < V)
+                    p.chunk[(int64_t)r * p.chunk_stride + e0 / G::CHUNK_EL] =
+                        (uint16_t)(key_of(CM::value(m[i])) >> 16);
+            }
         }
     } else {
-        float m = Vec16<T>::vmax(v[0]);
+        float m = -INFINITY;
 #pragma unroll
-        for (int i = 1; i < ROUNDS; ++i) m = fmax_nan(m, Vec16<T>::vmax(v[i]));
-        m = block_max_nan(m, redf);
+        for (int i = 0; i < G::ROUNDS; ++i) m = fmax_nan(m, Vec16<T>::vmax(fetch(i)));
+        m = group_max_nan<NTH>(m, redf, lt, sync);
         float s = 0.f;
         if (m > -INFINITY && m < INFINITY) {
 #pragma unroll
-            for (int i = 0; i < ROUNDS; ++i) s += Vec16<T>::vsumexp(v[i], m, p.c);
+            for (int i = 0; i < G::ROUNDS; ++i) s += Vec16<T>::vsumexp(fetch(i), m, p.c);
         }
-        const double tot = block_sum_d((double)s, redd);
-        if (threadIdx.x == 0) {
+        const double tot = group_sum_d<NTH>((double)s, redd, lt, sync);
+        if (lt == 0) {
             SegStat st;
             st.m = m;
             st.pad = 0.f;
@@ -175,14 +194,13 @@ struct SelCfg {
 __device__ __forceinline__ unsigned long long sel_weight(const SelCfg& cfg, float l)
 {
     if (!cfg.mass) return 1ull;
-    const float w = ex2_fast((l - cfg.M) * cfg.c) * cfg.scale;
-    return __float2ull_rn(w);
+    return __float2ull_rn(ex2_fast((l - cfg.M) * cfg.c) * cfg.scale);
 }
 
 // Finds the rank prefix {key > kappa} + {key == kappa, id <= i_kappa} whose last
 // token is where the inclusive cumulative weight (from the top rank) first
 // reaches `need`.  Returns false when the total weight is below `need` (then
-// every token is kept).
+// every token is kept).  hist: NBINS u64 of shared scratch.
 template <typename T>
 __device__ bool select_prefix(const T* row, int V, const SelCfg& cfg, unsigned long long need,
                               unsigned long long* hist, uint32_t* kappa_out, int32_t* ikappa_out)
@@ -190,7 +208,6 @@ __device__ bool select_prefix(const T* row, int V, const SelCfg& cfg, unsigned l
     __shared__ unsigned long long s_red[NT / 32 + 1];
     __shared__ unsigned long long s_cum;
     __shared__ uint32_t s_bin;
-    __shared__ int s_found;
     __shared__ int32_t s_ik;
     uint32_t pmask = 0, pval = 0;
     constexpr bool BF = sizeof(T) == 2;
@@ -199,8 +216,7 @@ __device__ bool select_prefix(const T* row, int V, const SelCfg& cfg, unsigned l
         const int shift = lev == 0 ? 21 : (lev == 1 ? 10 : 0);
         const int nb = lev == 2 ? 1024 : 2048;
         for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0ull;
-        if (threadIdx.x == 0) s_found = 0;
-        __syncthreads();
+        csync();
         for (int e = threadIdx.x; e < V; e += NT) {
             const float l = Elem<T>::load_cg(row, e);
             const uint32_t k = key_of(l);
@@ -209,28 +225,27 @@ __device__ bool select_prefix(const T* row, int V, const SelCfg& cfg, unsigned l
             const unsigned long long w = sel_weight(cfg, l);
             if (w) atomicAdd(&hist[(k >> shift) & (uint32_t)(nb - 1)], w);
         }
-        __syncthreads();
+        csync();
         const int per = nb / NT;
         unsigned long long local = 0;
         for (int q = 0; q < per; ++q) local += hist[nb - 1 - (threadIdx.x * per + q)];
         unsigned long long total;
         unsigned long long cum = block_excl_scan<unsigned long long>(local, s_red, &total);
-        if (total < need) return false;  // uniform across the block
+        if (total < need) return false;  // uniform across the compute threads
         for (int q = 0; q < per; ++q) {
             const int h = nb - 1 - (threadIdx.x * per + q);
             const unsigned long long w = hist[h];
             if (cum < need && need <= cum + w) {
                 s_bin = (uint32_t)h;
                 s_cum = cum;
-                s_found = 1;
             }
             cum += w;
         }
-        __syncthreads();
+        csync();
         need -= s_cum;
         pmask |= (uint32_t)(nb - 1) << shift;
         pval |= s_bin << shift;
-        __syncthreads();
+        csync();
     }
     uint32_t kappa = pval;
     if (BF) kappa |= (pval & 0x80000000u) ? 0u : 0x3FFu;  // bf16 keys end in 0s or 1s
@@ -268,12 +283,11 @@ __device__ bool select_prefix(const T* row, int V, const SelCfg& cfg, unsigned l
                     }
                 }
             }
-            __syncthreads();
             break;
         }
         running += total;
     }
-    __syncthreads();
+    csync();
     *kappa_out = kappa;
     *ikappa_out = s_ik < 0 ? V - 1 : s_ik;
     return true;
@@ -304,8 +318,7 @@ __device__ int collect_prefix(const T* row, int V, const RowStat& fin, float M, 
         for (int q = 0; q < WALK_EPT; ++q) {
             const int e = e0 + q;
             if (e >= V) break;
-            const float l = Elem<T>::load_cg(row, e);
-            if (kept_prefix(fin, key_of(l), e)) ++cnt;
+            if (kept_prefix(fin, key_of(Elem<T>::load_cg(row, e)), e)) ++cnt;
         }
         int total;
         int off = offset + block_excl_scan<int>(cnt, s_red_i, &total);
@@ -329,15 +342,317 @@ __device__ int collect_prefix(const T* row, int V, const RowStat& fin, float M, 
 }
 
 // ------------------------------------------------------------------------- //
+// fast top-k from the chunk-max keys.  The k-th largest chunk max is a lower  //
+// bound of the k-th largest key, so only chunks whose max reaches it can hold //
+// a kept token; they are re-read from L2 (about k chunks of 128 bytes).       //
+// Returns false when the candidates overflow (many ties): use the general     //
+// path.  On success fills st (MODE_LIST, or the nonfinite flag) and the       //
+// row's kept list.                                                           //
+// ------------------------------------------------------------------------- //
+constexpr int KEYQ = MAX_CHUNKS / 8 / NT;  // 16-byte words of chunk keys per thread
+constexpr int RANK_MAX = 256;              // counting-rank sort up to this size
+
+__device__ __forceinline__ int block_count(int v, int* red)
+{
+    v = __reduce_add_sync(0xffffffffu, v);
+    csync();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    csync();
+    int t = 0;
+#pragma unroll
+    for (int i = 0; i < NT / 32; ++i) t += red[i];
+    return t;
+}
+
+// sorts n distinct keys ascending from src into dst (shared): a counting rank
+// for small n, a bitonic sort in place (src == dst allowed only then) otherwise
+__device__ void sort_keys(const unsigned long long* src, unsigned long long* dst, int n)
+{
+    if (n <= RANK_MAX) {
+        for (int i = threadIdx.x; i < n; i += NT) {
+            const unsigned long long x = src[i];
+            int rk = 0;
+            for (int j = 0; j < n; ++j) rk += src[j] < x;
+            dst[rk] = x;
+        }
+        csync();
+        return;
+    }
+    const int n2 = next_pow2(n);
+    for (int i = threadIdx.x; i < n; i += NT) dst[i] = src[i];
+    for (int i = n + threadIdx.x; i < n2; i += NT) dst[i] = ~0ull;
+    csync();
+    bitonic_sort_u64(dst, n2);
+}
+
+// element q of a 16-byte word of T
+template <typename T> __device__ __forceinline__ float word_elem(uint4 w, int q);
+template <> __device__ __forceinline__ float word_elem<__nv_bfloat16>(uint4 w, int q)
+{
+    const uint32_t x = q < 2 ? w.x : q < 4 ? w.y : q < 6 ? w.z : w.w;
+    return (q & 1) ? bf16_hi(x) : bf16_lo(x);
+}
+template <> __device__ __forceinline__ float word_elem<float>(uint4 w, int q)
+{
+    return __uint_as_float(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
+}
+
+template <typename T>
+__device__ bool fast_topk(const Params& p, const T* row, int r, unsigned char* scratch,
+                          RowStat& st)
+{
+    __shared__ int s_cnt, s_nqual, s_flag, s_nk;
+    __shared__ int s_red_i[NT / 32 + 1];
+    __shared__ double s_redd[NT / 32 + 1];
+    unsigned long long* srt = (unsigned long long*)(scratch + SC_CK);   // sorted, CAND_CAP
+    unsigned long long* cand = (unsigned long long*)(scratch + SC_CAND);
+    int32_t* qual = (int32_t*)(scratch + SC_QUAL);
+    const int V = p.V, k = p.top_k, nc = p.nchunk;
+    const float c = p.c;
+    using G = SegGeom<T, NT>;
+
+    // chunk keys into registers, 8 per 16-byte load (row stride padded to 8)
+    const uint4* ckg = reinterpret_cast<const uint4*>(p.chunk + (int64_t)r * p.chunk_stride);
+    const int nw = (nc + 7) / 8;
+    uint4 kv[KEYQ];
+#pragma unroll
+    for (int q = 0; q < KEYQ; ++q) {
+        const int i = threadIdx.x + q * NT;
+        kv[q] = i < nw ? __ldcg(ckg + i) : make_uint4(0, 0, 0, 0);
+    }
+    // key e of word q of this thread (0 for padding: below every real key)
+    auto key_at = [&](int q, int e) -> uint32_t {
+        const int idx = (threadIdx.x + q * NT) * 8 + e;
+        const uint32_t w = e < 2 ? kv[q].x : e < 4 ? kv[q].y : e < 6 ? kv[q].z : kv[q].w;
+        return idx < nc ? ((w >> ((e & 1) * 16)) & 0xFFFFu) : 0u;
+    };
+    const int lane = threadIdx.x & 31;
+    uint32_t kmax = 0;
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < KEYQ; ++q)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t key = key_at(q, e);
+            kmax = max(kmax, key);
+            bad |= key >= 0xFF80u;  // +inf or NaN
+        }
+    if (threadIdx.x == 0) {
+        s_cnt = 0;
+        s_nqual = 0;
+    }
+    bad = csync_or(bad, &s_flag);
+    kmax = (uint32_t)__reduce_max_sync(0xffffffffu, kmax);
+    if ((threadIdx.x & 31) == 0) s_red_i[threadIdx.x >> 5] = (int)kmax;
+    csync();
+    kmax = 0;
+    for (int i = 0; i < NT / 32; ++i) kmax = max(kmax, (uint32_t)s_red_i[i]);
+    csync();
+    if (bad || kmax <= 0x007Fu) {  // NaN / +inf, or no finite logit
+        st.flags = FLAG_NONFINITE;
+        return true;
+    }
+    // tau16 = max{t : count(key >= t) >= k}, one 4-bit digit per level: 15
+    // counts per level, per-warp sums in a double-buffered table, no atomics
+    const int warp = threadIdx.x >> 5;
+    const int wbase = warp * 32;  // first key word of this warp at q = 0
+    uint32_t tau16 = 0;
+    {
+        __shared__ int s_cnt15[2][NT / 32][16];
+        for (int lev = 0; lev < 4; ++lev) {
+            const int shift = 12 - 4 * lev;
+            int cnt[15];
+#pragma unroll
+            for (int d = 0; d < 15; ++d) cnt[d] = 0;
+#pragma unroll
+            for (int q = 0; q < KEYQ; ++q) {
+                if (wbase + q * NT >= nw) continue;  // warp-uniform: no keys here
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t key = key_at(q, e);
+#pragma unroll
+                    for (int d = 0; d < 15; ++d) cnt[d] += key >= tau16 + ((uint32_t)(d + 1) << shift);
+                }
+            }
+#pragma unroll
+            for (int d = 0; d < 15; ++d) {
+                const int w = __reduce_add_sync(0xffffffffu, cnt[d]);
+                if (lane == d) s_cnt15[lev & 1][warp][d] = w;
+            }
+            csync();
+            int dsel = 0;
+#pragma unroll
+            for (int d = 0; d < 15; ++d) {
+                int t = 0;
+#pragma unroll
+                for (int wi = 0; wi < NT / 32; ++wi) t += s_cnt15[lev & 1][wi][d];
+                if (t >= k) dsel = d + 1;  // counts fall with d: the last that holds
+            }
+            tau16 += (uint32_t)dsel << shift;
+        }
+    }
+    const uint32_t tau32 = tau16 << 16;
+    // chunks that can hold a kept token, in ascending chunk order (block scan)
+    {
+        int mine = 0;
+#pragma unroll
+        for (int q = 0; q < KEYQ; ++q)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t key = key_at(q, e);
+                mine += key >= tau16 && key > 0;
+            }
+        int tot;
+        int off = block_excl_scan<int>(mine, s_red_i, &tot);
+        if (threadIdx.x == 0) s_nqual = tot;
+#pragma unroll
+        for (int q = 0; q < KEYQ; ++q)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t key = key_at(q, e);
+                if (key >= tau16 && key > 0) {
+                    if (off < CAND_CAP) qual[off] = (threadIdx.x + q * NT) * 8 + e;
+                    ++off;
+                }
+            }
+    }
+    csync();
+    const int nq = s_nqual;
+    if (nq > CAND_CAP) return false;
+
+    // gather: the qualifying chunks as 16-byte words, all loads in flight at once
+    constexpr int WPC = CHUNK_BYTES / 16;           // words per chunk
+    constexpr int EPW = 16 / (int)sizeof(T);        // elements per word
+    const int nwords = nq * WPC;
+    const char* rowb = (const char*)row;
+    const bool aligned = ((uintptr_t)row & 15u) == 0;  // else: element loads
+    uint4 gw[4];
+    int gi[4];
+    for (int base = 0; base < nwords; base += NT * 4) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int wi = base + g * NT + threadIdx.x;
+            gi[g] = -1;
+            gw[g] = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+            if (wi < nwords) {
+                const int e0 = qual[wi / WPC] * G::CHUNK_EL + (wi % WPC) * EPW;
+                if (e0 < V) {
+                    gi[g] = e0;
+                    if (aligned)
+                        gw[g] = __ldcg(reinterpret_cast<const uint4*>(rowb + (int64_t)e0 * (int64_t)sizeof(T)));
+                    else
+                        gw[g] = Vec16<T>::load_scalar(row, e0, V);
+                }
+            }
+        }
+        int cnt = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int q = 0; q < EPW; ++q)
+                cnt += gi[g] >= 0 && gi[g] + q < V && key_of(word_elem<T>(gw[g], q)) >= tau32;
+        int tot;
+        int off = s_cnt + block_excl_scan<int>(cnt, s_red_i, &tot);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int q = 0; q < EPW; ++q) {
+                const uint32_t key = key_of(word_elem<T>(gw[g], q));
+                if (gi[g] >= 0 && gi[g] + q < V && key >= tau32) {
+                    if (off < CAND_CAP)
+                        cand[off] = ((unsigned long long)(~key) << 32) | (uint32_t)(gi[g] + q);
+                    ++off;
+                }
+            }
+        csync();
+        if (threadIdx.x == 0) s_cnt += tot;
+        csync();
+    }
+    const int n = s_cnt;
+    if (n > CAND_CAP) return false;
+
+    // exact order: key descending, then id ascending
+    sort_keys(cand, srt, n);
+    const int kk = min(k, n);
+    const float M = val_of(~(uint32_t)(srt[0] >> 32));
+    // sum over the kept ranks by warp 0 (no block barrier)
+    __shared__ double s_S;
+    if (threadIdx.x < 32) {
+        float e_loc = 0.f;
+        for (int i = lane; i < kk; i += 32) e_loc += ex2_fast((val_of(~(uint32_t)(srt[i] >> 32)) - M) * c);
+        const double t = warp_sum_d((double)e_loc);
+        if (lane == 0) s_S = t;
+    }
+    csync();
+    double S = s_S;
+    int nk = kk;
+    if (p.top_p < 1.0f) {
+        // strict prefix rule over the kept ranks, in fp64 (one warp scans)
+        if (threadIdx.x < 32) {
+            double pre = 0.0;
+            int stop = kk;
+            for (int b0 = 0; b0 < kk; b0 += 32) {
+                const int i = b0 + lane;
+                const double pv =
+                    i < kk ? (double)ex2_fast((val_of(~(uint32_t)(srt[i] >> 32)) - M) * c) / S : 0.0;
+                double x = pv;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                const double before = pre + (x - pv);  // mass strictly before rank i
+                const unsigned drop =
+                    __ballot_sync(0xffffffffu, i < kk && !(before < (double)p.top_p));
+                if (drop) {
+                    stop = b0 + __ffs(drop) - 1;
+                    break;
+                }
+                pre += __shfl_sync(0xffffffffu, x, 31);
+            }
+            if (lane == 0) s_nk = stop;
+        }
+        csync();
+        nk = s_nk;
+        if (threadIdx.x < 32) {
+            float e2 = 0.f;
+            for (int i = lane; i < nk; i += 32) e2 += ex2_fast((val_of(~(uint32_t)(srt[i] >> 32)) - M) * c);
+            const double t = warp_sum_d((double)e2);
+            if (lane == 0) s_S = t;
+        }
+        csync();
+        S = s_S;
+    }
+    // the kept list in ascending id: re-key as (id << 32 | key) and sort again
+    for (int i = threadIdx.x; i < nk; i += NT) {
+        const unsigned long long x = srt[i];
+        cand[i] = ((unsigned long long)(uint32_t)x << 32) | (uint32_t)(~(uint32_t)(x >> 32));
+    }
+    csync();
+    sort_keys(cand, srt, nk);
+    int32_t* kid = p.kept_id + (int64_t)r * KCAP;
+    float* kl = p.kept_l + (int64_t)r * KCAP;
+    for (int i = threadIdx.x; i < nk; i += NT) {
+        const unsigned long long x = srt[i];
+        kid[i] = (int32_t)(x >> 32);
+        kl[i] = val_of((uint32_t)x);
+    }
+    st.M = M;
+    st.S = S;
+    st.n_kept = nk;
+    st.mode = MODE_LIST;
+    return true;
+}
+
+// ------------------------------------------------------------------------- //
 // row merge: statistics and kept set of row slot r                          //
 // ------------------------------------------------------------------------- //
 template <typename T>
-__device__ void merge_row(const Params& p, const T* row, int r, const Smem& sm)
+__device__ void merge_row(const Params& p, const T* row, int r, unsigned char* scratch)
 {
     __shared__ float s_redf[NT / 32 + 1];
     __shared__ double s_redd[NT / 32 + 1];
     __shared__ RowStat s_st;
-    __shared__ int s_cnt, s_nqual, s_fallback, s_nk;
     const int V = p.V;
     const float c = p.c;
     int32_t* kid = p.kept_id + (int64_t)r * KCAP;
@@ -357,169 +672,13 @@ __device__ void merge_row(const Params& p, const T* row, int r, const Smem& sm)
     bool done = false;
 
     if (p.seg_mode == SEG_CHUNK) {
-        // ---- fast top-k: the k-th largest chunk max bounds the k-th largest key
-        const int nc = p.nchunk;
-        const uint16_t* ckg = p.chunk + (int64_t)r * nc;
-        uint32_t kmax = 0;
-        bool bad = false;
-        for (int i = threadIdx.x; i < nc; i += NT) {
-            const uint16_t k = __ldcg(ckg + i);
-            sm.ck[i] = k;
-            kmax = max(kmax, (uint32_t)k);
-            bad |= (k >= 0xFF80u);  // +inf or NaN
-        }
-        for (int i = threadIdx.x; i < 256; i += NT) {
-            sm.h0[i] = 0;
-            sm.h1[i] = 0;
-        }
-        if (threadIdx.x == 0) {
-            s_cnt = 0;
-            s_nqual = 0;
-            s_fallback = 0;
-        }
-        bad = __syncthreads_or(bad);
-        kmax = (uint32_t)__reduce_max_sync(0xffffffffu, kmax);
-        __shared__ uint32_t s_kmax[NT / 32];
-        if ((threadIdx.x & 31) == 0) s_kmax[threadIdx.x >> 5] = kmax;
-        __syncthreads();
-        kmax = 0;
-        for (int i = 0; i < NT / 32; ++i) kmax = max(kmax, s_kmax[i]);
-        if (bad || kmax <= 0x007Fu) {  // NaN / +inf, or no finite logit
-            st.flags = FLAG_NONFINITE;
-            done = true;
-        } else {
-            // radix select of the k-th largest 16-bit chunk key (two byte digits)
-            const int k = p.top_k;
-            for (int i = threadIdx.x; i < nc; i += NT) atomicAdd(&sm.h0[sm.ck[i] >> 8], 1u);
-            __syncthreads();
-            __shared__ uint32_t s_hi, s_lo, s_need;
-            __shared__ int s_red_i[NT / 32 + 1];
-            {
-                const uint32_t cnt = sm.h0[255 - threadIdx.x];
-                int total;
-                const int ex = block_excl_scan<int>((int)cnt, s_red_i, &total);
-                if (ex < k && k <= ex + (int)cnt) {
-                    s_hi = 255 - threadIdx.x;
-                    s_need = k - ex;
-                }
-            }
-            __syncthreads();
-            const uint32_t hi = s_hi;
-            for (int i = threadIdx.x; i < nc; i += NT)
-                if ((uint32_t)(sm.ck[i] >> 8) == hi) atomicAdd(&sm.h1[sm.ck[i] & 255], 1u);
-            __syncthreads();
-            {
-                const int need = (int)s_need;
-                const uint32_t cnt = sm.h1[255 - threadIdx.x];
-                int total;
-                const int ex = block_excl_scan<int>((int)cnt, s_red_i, &total);
-                if (ex < need && need <= ex + (int)cnt) s_lo = 255 - threadIdx.x;
-            }
-            __syncthreads();
-            const uint32_t tau16 = (hi << 8) | s_lo;
-            const uint32_t tau32 = tau16 << 16;
-            // chunks that can hold a top-k token
-            for (int i = threadIdx.x; i < nc; i += NT)
-                if (sm.ck[i] >= tau16) {
-                    const int q = atomicAdd(&s_nqual, 1);
-                    if (q < CAND_CAP) sm.qual[q] = i;
-                }
-            __syncthreads();
-            const int nq = s_nqual;
-            if (nq > CAND_CAP) {
-                s_fallback = 1;
-            } else {
-                constexpr int CHUNK_EL = CHUNK_BYTES / (int)sizeof(T);
-                const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-                for (int q = w; q < nq; q += NT / 32) {
-                    const int e_base = sm.qual[q] * CHUNK_EL;
-                    for (int e = e_base + lane; e < e_base + CHUNK_EL; e += 32) {
-                        bool take = false;
-                        uint32_t key = 0;
-                        if (e < V) {
-                            key = key_of(Elem<T>::load_cg(row, e));
-                            take = key >= tau32;
-                        }
-                        const unsigned bal = __ballot_sync(0xffffffffu, take);
-                        int slot0 = 0;
-                        if (lane == 0 && bal) slot0 = atomicAdd(&s_cnt, __popc(bal));
-                        slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-                        if (take) {
-                            const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-                            if (slot < CAND_CAP)
-                                sm.cand[slot] = ((unsigned long long)(~key) << 32) | (uint32_t)e;
-                        }
-                    }
-                }
-                __syncthreads();
-                if (s_cnt > CAND_CAP) s_fallback = 1;
-            }
-            __syncthreads();
-            if (!s_fallback) {
-                // exact order: key descending, then id ascending
-                const int n = s_cnt;
-                const int n2 = next_pow2(n);
-                for (int i = n + threadIdx.x; i < n2; i += NT) sm.cand[i] = ~0ull;
-                __syncthreads();
-                bitonic_sort_u64(sm.cand, n2);
-                const int kk = min(k, n);
-                const float M = val_of(~(uint32_t)(sm.cand[0] >> 32));
-                // exponentials of the kept ranks (rank order) and their sum
-                float e_loc = 0.f;
-                for (int i = threadIdx.x; i < kk; i += NT) {
-                    const float l = val_of(~(uint32_t)(sm.cand[i] >> 32));
-                    e_loc += ex2_fast((l - M) * c);
-                }
-                double S = block_sum_d((double)e_loc, s_redd);
-                int nk = kk;
-                if (topp_on) {
-                    // strict prefix rule over the kept ranks, in fp64
-                    if (threadIdx.x == 0) {
-                        double pre = 0.0;
-                        int i = 0;
-                        for (; i < kk; ++i) {
-                            if (!(pre < (double)p.top_p)) break;
-                            const float l = val_of(~(uint32_t)(sm.cand[i] >> 32));
-                            pre += (double)ex2_fast((l - M) * c) / S;
-                        }
-                        s_nk = i;
-                    }
-                    __syncthreads();
-                    nk = s_nk;
-                    float e2 = 0.f;
-                    for (int i = threadIdx.x; i < nk; i += NT) {
-                        const float l = val_of(~(uint32_t)(sm.cand[i] >> 32));
-                        e2 += ex2_fast((l - M) * c);
-                    }
-                    S = block_sum_d((double)e2, s_redd);
-                }
-                // the kept list in ascending id: re-key as (id << 32 | key)
-                __syncthreads();
-                for (int i = threadIdx.x; i < nk; i += NT) {
-                    const unsigned long long x = sm.cand[i];
-                    sm.cand[i] = ((unsigned long long)(uint32_t)x << 32) | (uint32_t)(~(uint32_t)(x >> 32));
-                }
-                const int nk2 = next_pow2(nk);
-                for (int i = nk + threadIdx.x; i < nk2; i += NT) sm.cand[i] = ~0ull;
-                __syncthreads();
-                bitonic_sort_u64(sm.cand, nk2);
-                for (int i = threadIdx.x; i < nk; i += NT) {
-                    const unsigned long long x = sm.cand[i];
-                    kid[i] = (int32_t)(x >> 32);
-                    kl[i] = val_of((uint32_t)x);
-                }
-                st.M = M;
-                st.S = S;
-                st.n_kept = nk;
-                st.mode = MODE_LIST;
-                done = true;
-            }
-        }
-        __syncthreads();
+        done = fast_topk<T>(p, row, r, scratch, st);
+        csync();
     } else {
-        // ---- statistics over all tokens from the segment records
+        // statistics over all tokens from the segment records
         float m = -INFINITY;
-        for (int i = threadIdx.x; i < p.nseg; i += NT) m = fmax_nan(m, __ldcg(&p.seg[(int64_t)r * p.nseg + i].m));
+        for (int i = threadIdx.x; i < p.nseg; i += NT)
+            m = fmax_nan(m, __ldcg(&p.seg[(int64_t)r * p.nseg + i].m));
         const float M = block_max_nan(m, s_redf);
         if (!(M > -INFINITY && M < INFINITY)) {
             st.flags = FLAG_NONFINITE;
@@ -529,7 +688,8 @@ __device__ void merge_row(const Params& p, const T* row, int r, const Smem& sm)
             for (int i = threadIdx.x; i < p.nseg; i += NT) {
                 const SegStat* g = p.seg + (int64_t)r * p.nseg + i;
                 const float gm = __ldcg(&g->m);
-                if (gm > -INFINITY) s += __ldcg(&g->s) * exp2(((double)gm - (double)M) * (double)c);
+                if (gm > -INFINITY)
+                    s += __ldcg(&g->s) * exp2(((double)gm - (double)M) * (double)c);
             }
             st.M = M;
             st.S = block_sum_d(s, s_redd);
@@ -539,127 +699,150 @@ __device__ void merge_row(const Params& p, const T* row, int r, const Smem& sm)
     }
 
     if (!done) {
-        // ---- general path: radix descent over the full row (read from L2)
-        if (!have_stats) st.M = row_max<T>(row, V, s_redf);
-        RowStat pre;  // the current kept rank prefix
-        pre.mode = MODE_ALL;
-        pre.kappa = 0;
-        pre.i_kappa = V - 1;
-        double S_pre = st.S;  // sum over the current kept set (valid if have_stats)
-        if (topk_on) {
-            SelCfg cfg;
-            cfg.mass = false;
-            cfg.M = st.M;
-            cfg.c = c;
-            cfg.scale = 0.f;
-            cfg.restricted = false;
-            uint32_t kap;
-            int32_t ik;
-            if (select_prefix<T>(row, V, cfg, (unsigned long long)p.top_k, sm.cand, &kap, &ik)) {
-                pre.mode = MODE_PREFIX;
-                pre.kappa = kap;
-                pre.i_kappa = ik;
-            }
-            // sum over the top-k set (the list is rewritten below)
-            collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S_pre);
-        } else if (!have_stats) {
-            collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S_pre);
+        // general path: radix descent over the full row (read from L2)
+        unsigned long long* hist = (unsigned long long*)scratch;
+        if (!have_stats) {
+            st.M = row_max<T>(row, V, s_redf);
+            if (!(st.M > -INFINITY && st.M < INFINITY)) st.flags = FLAG_NONFINITE;
         }
-        if (topp_on) {
-            SelCfg cfg;
-            cfg.mass = true;
-            cfg.M = st.M;
-            cfg.c = c;
-            cfg.scale = (float)(72057594037927936.0 / S_pre);  // 2^56 / S
-            cfg.restricted = pre.mode == MODE_PREFIX;
-            cfg.rst = pre;
-            uint32_t kap;
-            int32_t ik;
-            if (select_prefix<T>(row, V, cfg, p.top_p_fix, sm.cand, &kap, &ik)) {
-                pre.mode = MODE_PREFIX;
-                pre.kappa = kap;
-                pre.i_kappa = ik;
+        if (!st.flags) {
+            RowStat pre;  // the current kept rank prefix
+            pre.mode = MODE_ALL;
+            pre.kappa = 0;
+            pre.i_kappa = V - 1;
+            double S_pre = st.S;
+            if (topk_on) {
+                SelCfg cfg;
+                cfg.mass = false;
+                cfg.M = st.M;
+                cfg.c = c;
+                cfg.scale = 0.f;
+                cfg.restricted = false;
+                uint32_t kap;
+                int32_t ik;
+                if (select_prefix<T>(row, V, cfg, (unsigned long long)p.top_k, hist, &kap, &ik)) {
+                    pre.mode = MODE_PREFIX;
+                    pre.kappa = kap;
+                    pre.i_kappa = ik;
+                }
+                if (topp_on) collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S_pre);
             }
+            if (topp_on) {
+                SelCfg cfg;
+                cfg.mass = true;
+                cfg.M = st.M;
+                cfg.c = c;
+                cfg.scale = (float)(72057594037927936.0 / S_pre);  // 2^56 / S
+                cfg.restricted = pre.mode == MODE_PREFIX;
+                cfg.rst = pre;
+                uint32_t kap;
+                int32_t ik;
+                if (select_prefix<T>(row, V, cfg, p.top_p_fix, hist, &kap, &ik)) {
+                    pre.mode = MODE_PREFIX;
+                    pre.kappa = kap;
+                    pre.i_kappa = ik;
+                }
+            }
+            double S;
+            const int nk = collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S);
+            st.S = S;
+            st.n_kept = nk;
+            st.kappa = pre.kappa;
+            st.i_kappa = pre.i_kappa;
+            st.mode = nk <= KCAP ? MODE_LIST : (pre.mode == MODE_ALL ? MODE_ALL : MODE_PREFIX);
         }
-        double S;
-        const int nk = collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S);
-        st.S = S;
-        st.n_kept = nk;
-        st.kappa = pre.kappa;
-        st.i_kappa = pre.i_kappa;
-        st.mode = nk <= KCAP ? MODE_LIST : (pre.mode == MODE_ALL ? MODE_ALL : MODE_PREFIX);
     }
     if (threadIdx.x == 0) s_st = st;
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) p.rstat[r] = s_st;
 }
 
 // ------------------------------------------------------------------------- //
-// probability of one token under a merged row                               //
-// ------------------------------------------------------------------------- //
-template <typename T>
-__device__ float token_logit(const Params& p, int r, const RowStat& st, const T* row, int x, bool* kept)
-{
-    if (st.mode == MODE_LIST) {
-        const int32_t* ids = p.kept_id + (int64_t)r * KCAP;
-        const int i = lower_bound_i32(ids, st.n_kept, x);
-        *kept = i < st.n_kept && __ldcg(ids + i) == x;
-        return *kept ? __ldcg(p.kept_l + (int64_t)r * KCAP + i) : -INFINITY;
-    }
-    const float l = Elem<T>::load_cg(row, x);
-    *kept = kept_prefix(st, key_of(l), x);
-    return l;
-}
-
-// P(x) of a merged row, in fp32 with an accurate exponential
-template <typename T>
-__device__ float token_prob(const Params& p, int r, const RowStat& st, const T* row, int x)
-{
-    bool kept;
-    const float l = token_logit<T>(p, r, st, row, x, &kept);
-    if (!kept) return 0.f;
-    return (float)((double)exp2f((l - st.M) * p.c) / st.S);
-}
-
-// ------------------------------------------------------------------------- //
-// inverse CDF over an explicit kept list (ascending id), in this CTA        //
-// R(v) = max(0, P_t(v) - P_d(v)) for a residual, else P_t(v)                //
+// inverse CDF over the target's kept list (ascending id), in this CTA.       //
+// R(v) = max(0, P_t(v) - P_d(v)) for a residual, else P_t(v).  Both lists   //
+// are staged in shared scratch first.                                       //
 // ------------------------------------------------------------------------- //
 struct DraftRef {
-    int kind;           // 0: logits row (r >= 0), 1: probabilities row
+    int kind;           // 0: logits row (merged stats st), 1: probabilities row
     int r;
     RowStat st;
     const void* row;    // draft logits (T) or probabilities (float)
 };
 
+struct StagedList {
+    const int32_t* ids;
+    const float* ls;
+    int n;
+};
+
+__device__ __forceinline__ int lower_bound_smem(const int32_t* a, int n, int x)
+{
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
 template <typename T>
-__device__ __forceinline__ float draft_prob(const Params& p, const DraftRef& d, int v)
+__device__ __forceinline__ float staged_draft_prob(const Params& p, const DraftRef& d,
+                                                   const StagedList& dl, float invSd, int v)
 {
     if (d.kind == 1) return __ldcg((const float*)d.row + v);
-    return token_prob<T>(p, d.r, d.st, (const T*)d.row, v);
+    if (d.st.mode == MODE_LIST) {
+        const int i = lower_bound_smem(dl.ids, dl.n, v);
+        return (i < dl.n && dl.ids[i] == v) ? ex2_fast((dl.ls[i] - d.st.M) * p.c) * invSd : 0.f;
+    }
+    const float l = Elem<T>::load_cg((const T*)d.row, v);
+    return kept_prefix(d.st, key_of(l), v) ? ex2_fast((l - d.st.M) * p.c) * invSd : 0.f;
 }
 
 template <typename T>
-__device__ __forceinline__ unsigned long long list_r_fix(const Params& p, const RowStat& ts, float l,
-                                                         int v, bool residual, const DraftRef& d)
+__device__ __forceinline__ unsigned long long list_r_fix(const Params& p, const RowStat& ts,
+                                                         const StagedList& tl, int i, bool res,
+                                                         const DraftRef& d, const StagedList& dl,
+                                                         float invSt, float invSd)
 {
-    const float pt = ex2_fast((l - ts.M) * p.c) * (float)(1.0 / ts.S);
-    const float r = residual ? fmaxf(pt - draft_prob<T>(p, d, v), 0.f) : pt;
-    return to_fix56(r);
+    const float pt = ex2_fast((tl.ls[i] - ts.M) * p.c) * invSt;
+    const float rv = res ? fmaxf(pt - staged_draft_prob<T>(p, d, dl, invSd, tl.ids[i]), 0.f) : pt;
+    return to_fix56(rv);
 }
 
-// Inverse CDF over the target's kept list in ascending id.  Returns the token;
-// *Zfix the residual mass (2^-56 units) before any fallback; *zero when the
-// residual summed to 0 and the target row itself was sampled.
 template <typename T>
 __device__ int sample_list(const Params& p, int tr, const RowStat& ts, bool residual,
-                           const DraftRef& d, float u, unsigned long long* Zfix, bool* zero)
+                           const DraftRef& d, float u, unsigned char* scratch,
+                           unsigned long long* Zfix, bool* zero)
 {
     __shared__ unsigned long long s_red[NT / 32 + 1];
     __shared__ int s_tok;
     const int n = ts.n_kept;
-    const int32_t* ids = p.kept_id + (int64_t)tr * KCAP;
-    const float* ls = p.kept_l + (int64_t)tr * KCAP;
+    int32_t* ti = (int32_t*)scratch;
+    float* tv = (float*)(scratch + KCAP * 4);
+    int32_t* di = (int32_t*)(scratch + KCAP * 8);
+    float* dv = (float*)(scratch + KCAP * 12);
+    StagedList tl{ti, tv, n}, dl{di, dv, 0};
+    {
+        const int32_t* gi = p.kept_id + (int64_t)tr * KCAP;
+        const float* gv = p.kept_l + (int64_t)tr * KCAP;
+        for (int i = threadIdx.x; i < n; i += NT) {
+            ti[i] = __ldcg(gi + i);
+            tv[i] = __ldcg(gv + i);
+        }
+        if (residual && d.kind == 0 && d.st.mode == MODE_LIST) {
+            dl.n = d.st.n_kept;
+            const int32_t* hi = p.kept_id + (int64_t)d.r * KCAP;
+            const float* hv = p.kept_l + (int64_t)d.r * KCAP;
+            for (int i = threadIdx.x; i < dl.n; i += NT) {
+                di[i] = __ldcg(hi + i);
+                dv[i] = __ldcg(hv + i);
+            }
+        }
+        csync();
+    }
+    const float invSt = (float)(1.0 / ts.S);
+    const float invSd = (residual && d.kind == 0) ? (float)(1.0 / d.st.S) : 0.f;
     const int ept = (n + NT - 1) / NT;
     const int i0 = threadIdx.x * ept;
     *zero = false;
@@ -669,7 +852,7 @@ __device__ int sample_list(const Params& p, int tr, const RowStat& ts, bool resi
         for (int q = 0; q < ept; ++q) {
             const int i = i0 + q;
             if (i >= n) break;
-            part += list_r_fix<T>(p, ts, __ldcg(ls + i), __ldcg(ids + i), res, d);
+            part += list_r_fix<T>(p, ts, tl, i, res, d, dl, invSt, invSd);
         }
         unsigned long long Z;
         const unsigned long long ex = block_excl_scan<unsigned long long>(part, s_red, &Z);
@@ -683,20 +866,20 @@ __device__ int sample_list(const Params& p, int tr, const RowStat& ts, bool resi
         }
         const unsigned long long t = cdf_target(u, Z);
         if (threadIdx.x == 0) s_tok = -1;
-        __syncthreads();
+        csync();
         if (ex <= t && t < ex + part) {
             unsigned long long acc = ex;
             for (int q = 0; q < ept; ++q) {
                 const int i = i0 + q;
                 if (i >= n) break;
-                acc += list_r_fix<T>(p, ts, __ldcg(ls + i), __ldcg(ids + i), res, d);
+                acc += list_r_fix<T>(p, ts, tl, i, res, d, dl, invSt, invSd);
                 if (acc > t) {
-                    s_tok = __ldcg(ids + i);
+                    s_tok = tl.ids[i];
                     break;
                 }
             }
         }
-        __syncthreads();
+        csync();
         return s_tok;
     }
     return -1;
@@ -705,39 +888,80 @@ __device__ int sample_list(const Params& p, int tr, const RowStat& ts, bool resi
 // ------------------------------------------------------------------------- //
 // the decision of one sequence (verify launch)                              //
 // ------------------------------------------------------------------------- //
+constexpr int DECIDE_ROWS_OFF = 2 * KCAP * 8;  // staged row records after the two lists
+constexpr int MAX_DECIDE_ROWS = (SCRATCH_BYTES - DECIDE_ROWS_OFF) / (int)sizeof(RowStat);
+static_assert(MAX_DECIDE_ROWS >= 2 * 255 + 1, "row records of K_max = 255 must fit");
+
+// logit at token x of a merged row for one full warp: a kept list is scanned
+// in 32-wide stripes with every stripe of ids and values loaded at once
 template <typename T>
-__device__ void decide_sequence(const Params& p, int b)
+__device__ __forceinline__ float warp_lookup(const Params& p, int r, const RowStat& st, const T* row,
+                                             int x, bool* kept)
+{
+    const int lane = threadIdx.x & 31;
+    if (st.mode != MODE_LIST) {
+        const float l = Elem<T>::load_cg(row, x);
+        *kept = kept_prefix(st, key_of(l), x);
+        return l;
+    }
+    const int32_t* ids = p.kept_id + (int64_t)r * KCAP;
+    const float* ls = p.kept_l + (int64_t)r * KCAP;
+    const int n = st.n_kept;
+    for (int b0 = 0; b0 < n; b0 += 128) {
+        int v[4];
+        float w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = b0 + q * 32 + lane;
+            v[q] = i < n ? __ldcg(ids + i) : -1;
+            w[q] = i < n ? __ldcg(ls + i) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const unsigned m = __ballot_sync(0xffffffffu, v[q] == x);
+            if (m) {
+                *kept = true;
+                return __shfl_sync(0xffffffffu, w[q], __ffs(m) - 1);
+            }
+        }
+    }
+    *kept = false;
+    return -INFINITY;
+}
+
+template <typename T>
+__device__ void decide_sequence(const Params& p, int b, unsigned char* scratch)
 {
     __shared__ int s_jstar, s_bad, s_nonfinite;
+    RowStat* rs = reinterpret_cast<RowStat*>(scratch + DECIDE_ROWS_OFF);  // [target 0..K, draft 0..K-1]
     const int K = p.Kmax, V = p.V;
     const int kb = seq_k(p, b);
     const T* target = (const T*)p.target;
     const int64_t trow0 = (int64_t)b * (K + 1) * V;
     const int64_t drow0 = (int64_t)b * K * V;
+    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
     if (threadIdx.x == 0) {
         s_jstar = kb;
         s_bad = 0;
         s_nonfinite = 0;
     }
-    __syncthreads();
+    csync();
+    // one parallel round of loads: row records, drafted tokens (and q(x))
+    for (int i = threadIdx.x; i < nrows; i += NT) {
+        const int r = i <= kb ? target_slot(p, b, i) : draft_slot(p, b, i - kb - 1);
+        rs[i] = load_rowstat(p.rstat + r);
+        if (rs[i].flags & FLAG_NONFINITE) s_nonfinite = 1;
+    }
     for (int j = threadIdx.x; j < kb; j += NT) {
         const int x = p.xin[(int64_t)b * K + j];
-        if (x < 0 || x >= V) s_bad = 1;
-    }
-    for (int j = threadIdx.x; j <= kb; j += NT) {
-        if (load_rowstat(p.rstat + target_slot(p, b, j)).flags & FLAG_NONFINITE) s_nonfinite = 1;
-        if (j < kb && p.draft_kind == 0 && (load_rowstat(p.rstat + draft_slot(p, b, j)).flags & FLAG_NONFINITE))
-            s_nonfinite = 1;
-    }
-    __syncthreads();
-    if (!s_bad && p.draft_kind == 1) {
-        for (int j = threadIdx.x; j < kb; j += NT) {
-            const int x = p.xin[(int64_t)b * K + j];
+        if (x < 0 || x >= V) {
+            s_bad = 1;
+        } else if (p.draft_kind == 1) {
             const float q = __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x);
             if (!(q >= 0.f) || q == INFINITY) s_nonfinite = 1;
         }
     }
-    __syncthreads();
+    csync();
     if (s_bad || s_nonfinite) {
         for (int j = threadIdx.x; j <= K; j += NT) {
             p.tokens[(int64_t)b * (K + 1) + j] = -1;
@@ -755,42 +979,40 @@ __device__ void decide_sequence(const Params& p, int b)
         }
         return;
     }
-    // accept tests of every slot (independent), first rejection by a min
-    for (int j = threadIdx.x; j < kb; j += NT) {
+    // accept tests of every slot (one warp per slot), first rejection by a min
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < kb; j += NT / 32) {
         const int x = p.xin[(int64_t)b * K + j];
-        const int tr = target_slot(p, b, j);
-        const RowStat ts = load_rowstat(p.rstat + tr);
-        const float pt = token_prob<T>(p, tr, ts, target + trow0 + (int64_t)j * V, x);
+        const RowStat ts = rs[j];
+        bool kt, kd = true;
+        const float lt = warp_lookup<T>(p, target_slot(p, b, j), ts, target + trow0 + (int64_t)j * V, x, &kt);
         float pd;
         if (p.draft_kind == 1) {
             pd = __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x);
         } else {
-            const int dr = draft_slot(p, b, j);
-            pd = token_prob<T>(p, dr, load_rowstat(p.rstat + dr), (const T*)p.draft + drow0 + (int64_t)j * V, x);
+            const RowStat ds = rs[kb + 1 + j];
+            const float ld = warp_lookup<T>(p, draft_slot(p, b, j), ds,
+                                            (const T*)p.draft + drow0 + (int64_t)j * V, x, &kd);
+            pd = kd ? (float)((double)exp2f((ld - ds.M) * p.c) / ds.S) : 0.f;
         }
-        const uint4 w = slot_words(p, b, j, 0u);
-        const float u_acc = u24(w.x);
-        const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
-        const bool accept = (double)u_acc < ratio;
-        if (!accept) atomicMin(&s_jstar, j);
-        if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = pt;
-        if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = pd;
+        const float pt = kt ? (float)((double)exp2f((lt - ts.M) * p.c) / ts.S) : 0.f;
+        if (lane == 0) {
+            const uint4 w = slot_words(p, b, j, 0u);
+            const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
+            if (!((double)u24(w.x) < ratio)) atomicMin(&s_jstar, j);
+            if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = pt;
+            if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = pd;
+        }
     }
     for (int j = threadIdx.x; j <= K; j += NT) {
-        if (p.lse) {
-            float v = NAN;
-            if (j <= kb) {
-                const RowStat ts = load_rowstat(p.rstat + target_slot(p, b, j));
-                v = (float)((double)ts.M / (double)p.T + log(ts.S));
-            }
-            p.lse[(int64_t)b * (K + 1) + j] = v;
-        }
+        if (p.lse) p.lse[(int64_t)b * (K + 1) + j] =
+            j <= kb ? (float)((double)rs[j].M / (double)p.T + log(rs[j].S)) : NAN;
         if (j >= kb && j < K) {
             if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
             if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = NAN;
         }
     }
-    __syncthreads();
+    csync();
     const int jstar = s_jstar;
     for (int j = threadIdx.x; j <= K; j += NT)
         p.tokens[(int64_t)b * (K + 1) + j] = (j < jstar) ? p.xin[(int64_t)b * K + j] : -1;
@@ -798,7 +1020,7 @@ __device__ void decide_sequence(const Params& p, int b)
     const uint4 w = slot_words(p, b, jstar, 0u);
     const float u = u24(w.y);
     const int tr = target_slot(p, b, jstar);
-    const RowStat ts = load_rowstat(p.rstat + tr);
+    const RowStat ts = rs[jstar];
     if (threadIdx.x == 0) {
         p.num_accepted[b] = jstar;
         if (p.row_status) p.row_status[b] = ROW_OK;
@@ -807,14 +1029,15 @@ __device__ void decide_sequence(const Params& p, int b)
     DraftRef d;
     d.kind = p.draft_kind;
     d.r = residual ? draft_slot(p, b, jstar) : -1;
-    if (residual && d.kind == 0) d.st = load_rowstat(p.rstat + d.r);
-    d.row = residual ? (const void*)((const char*)p.draft + (drow0 + (int64_t)jstar * V) *
-                                                            (d.kind == 1 ? 4 : (int64_t)sizeof(T)))
+    if (residual && d.kind == 0) d.st = rs[kb + 1 + jstar];
+    d.row = residual ? (const void*)((const char*)p.draft +
+                                     (drow0 + (int64_t)jstar * V) * (d.kind == 1 ? 4 : (int64_t)sizeof(T)))
                      : nullptr;
+    csync();  // the row records are read; sample_list reuses the front of the scratch
     if (ts.mode == MODE_LIST) {
         unsigned long long Z;
         bool zero;
-        const int tok = sample_list<T>(p, tr, ts, residual, d, u, &Z, &zero);
+        const int tok = sample_list<T>(p, tr, ts, residual, d, u, scratch, &Z, &zero);
         if (threadIdx.x == 0) {
             p.tokens[(int64_t)b * (K + 1) + jstar] = tok;
             if (residual && p.resid_mass) p.resid_mass[b] = (float)from_fix56(Z);
@@ -835,15 +1058,14 @@ __device__ void decide_sequence(const Params& p, int b)
 
 // the draft-side sampler: sample row r from its own distribution (tag 1)
 template <typename T>
-__device__ void sample_own_row(const Params& p, int r, const RowRef& rr)
+__device__ void sample_own_row(const Params& p, int r, const RowRef& rr, unsigned char* scratch)
 {
     const RowStat st = load_rowstat(p.rstat + r);
     const int out = rr.b * p.Kmax + rr.j;
-    const int jidx = rr.b * p.Kmax + rr.j;  // one job slot per draft row
     if (st.flags & FLAG_NONFINITE) {
         if (threadIdx.x == 0) {
             p.tokens[out] = -1;
-            p.jobs[jidx].kind = JOB_NONE;
+            p.jobs[out].kind = JOB_NONE;
         }
         return;
     }
@@ -856,10 +1078,10 @@ __device__ void sample_own_row(const Params& p, int r, const RowRef& rr)
         d.row = nullptr;
         unsigned long long Z;
         bool zero;
-        const int tok = sample_list<T>(p, r, st, false, d, u, &Z, &zero);
+        const int tok = sample_list<T>(p, r, st, false, d, u, scratch, &Z, &zero);
         if (threadIdx.x == 0) {
             p.tokens[out] = tok;
-            p.jobs[jidx].kind = JOB_NONE;
+            p.jobs[out].kind = JOB_NONE;
         }
     } else if (threadIdx.x == 0) {
         Job jb;
@@ -869,104 +1091,306 @@ __device__ void sample_own_row(const Params& p, int r, const RowRef& rr)
         jb.out_idx = out;
         jb.b = rr.b;
         jb.u = u;
-        p.jobs[jidx] = jb;
+        p.jobs[out] = jb;
     }
 }
 
+// outputs of a row slot that is not read: a sequence with K_b outside
+// [0, K_max] (reported by its first slot), or a draft slot beyond K_b
+__device__ void report_skipped_row(const Params& p, const RowRef& rr)
+{
+    const int K = p.Kmax;
+    if (!k_ok(p, rr.kb)) {
+        const bool first = p.draft_launch ? rr.j == 0 : (!rr.is_draft && rr.j == 0);
+        if (!first) return;
+        if (p.draft_launch) {
+            for (int j = 0; j < K; ++j) {
+                p.tokens[(int64_t)rr.b * K + j] = -1;
+                p.jobs[rr.b * K + j].kind = JOB_NONE;
+            }
+        } else {
+            for (int j = 0; j <= K; ++j) {
+                p.tokens[(int64_t)rr.b * (K + 1) + j] = -1;
+                if (p.lse) p.lse[(int64_t)rr.b * (K + 1) + j] = NAN;
+                if (j < K && p.p_t_at) p.p_t_at[(int64_t)rr.b * K + j] = NAN;
+                if (j < K && p.p_d_at) p.p_d_at[(int64_t)rr.b * K + j] = NAN;
+            }
+            p.num_accepted[rr.b] = -1;
+            if (p.row_status) p.row_status[rr.b] = ROW_BAD_K;
+            if (p.resid_mass) p.resid_mass[rr.b] = NAN;
+            p.jobs[rr.b].kind = JOB_NONE;
+        }
+    } else if (p.draft_launch) {
+        p.tokens[(int64_t)rr.b * K + rr.j] = -1;
+        p.jobs[rr.b * K + rr.j].kind = JOB_NONE;
+    }
+}
+
+// Row r, every segment streamed: merge it; then (draft launch) sample it, or
+// (verify) take the sequence ticket, and the last row of the sequence decides
+// it.  Called by NT threads; only thread 0 fences and takes the ticket.
+template <typename T>
+__device__ void finish_row(const Params& p, int r, const RowRef& rr, const T* row,
+                           unsigned char* scratch)
+{
+    __shared__ int s_last_seq;
+    merge_row<T>(p, row, r, scratch);
+    if (p.draft_launch) {
+        csync();
+        if (threadIdx.x == 0) __threadfence();
+        csync();
+        sample_own_row<T>(p, r, rr, scratch);
+        return;
+    }
+    csync();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
+        s_last_seq = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
+        if (s_last_seq) {
+            __threadfence();
+            p.seq_ticket[rr.b] = 0u;
+        }
+    }
+    csync();
+    if (!s_last_seq) return;
+    decide_sequence<T>(p, rr.b, scratch);
+}
+
 // ------------------------------------------------------------------------- //
-// stage-1 kernel: one CTA per (row slot, segment)                           //
+// k_rows: one CTA per (row slot, segment), loads straight into registers     //
+// (rows that do not start on a 16-byte boundary)                             //
 // ------------------------------------------------------------------------- //
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(NT, 4) k_rows(const Params p)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ float s_redf[NT / 32 + 1];
     __shared__ double s_redd[NT / 32 + 1];
-    __shared__ int s_last;
+    using G = SegGeom<T, NT>;
     const int r = blockIdx.x / p.nseg;
     const int seg = blockIdx.x - r * p.nseg;
     const RowRef rr = row_ref(p, r);
     if (!rr.valid) {
-        if (seg == 0 && threadIdx.x == 0) {
-            const int K = p.Kmax;
-            if (!k_ok(p, rr.kb)) {
-                // a sequence with K_b outside [0, K_max]: reported by its first slot
-                const bool first = p.draft_launch ? rr.j == 0 : (!rr.is_draft && rr.j == 0);
-                if (first) {
-                    if (p.draft_launch) {
-                        for (int j = 0; j < K; ++j) p.tokens[(int64_t)rr.b * K + j] = -1;
-                    } else {
-                        for (int j = 0; j <= K; ++j) {
-                            p.tokens[(int64_t)rr.b * (K + 1) + j] = -1;
-                            if (p.lse) p.lse[(int64_t)rr.b * (K + 1) + j] = NAN;
-                            if (j < K && p.p_t_at) p.p_t_at[(int64_t)rr.b * K + j] = NAN;
-                            if (j < K && p.p_d_at) p.p_d_at[(int64_t)rr.b * K + j] = NAN;
-                        }
-                        p.num_accepted[rr.b] = -1;
-                        if (p.row_status) p.row_status[rr.b] = ROW_BAD_K;
-                        if (p.resid_mass) p.resid_mass[rr.b] = NAN;
-                        p.jobs[rr.b].kind = JOB_NONE;
-                    }
-                }
-            } else if (p.draft_launch) {
-                p.tokens[(int64_t)rr.b * K + rr.j] = -1;  // slot beyond K_b
-                p.jobs[rr.b * K + rr.j].kind = JOB_NONE;
-            }
-        }
+        if (seg == 0 && threadIdx.x == 0) report_skipped_row(p, rr);
         return;
     }
     if (rr.is_draft && p.draft_kind == 1) return;  // probabilities: read only where needed
 
-    const T* base = (const T*)(rr.is_draft ? p.draft : p.target);
-    const T* row = base + row_elem_offset(p, rr);
-    segment_pass<T, VEC, MODE>(p, row, seg, r, s_redf, s_redd);
-
-    // last segment of the row merges it
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(&p.row_ticket[r], 1u) == (unsigned)(p.nseg - 1));
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) p.row_ticket[r] = 0u;
-    const Smem sm = smem_layout(smem_raw);
-    merge_row<T>(p, row, r, sm);
-
-    if (p.draft_launch) {
-        __threadfence();
-        __syncthreads();
-        sample_own_row<T>(p, r, rr);
-        return;
+    const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
+    const int64_t base = (int64_t)seg * G::SEG;
+    uint4 v[G::ROUNDS];
+#pragma unroll
+    for (int i = 0; i < G::ROUNDS; ++i) {
+        const int64_t e0 = base + ((int64_t)i * NT + threadIdx.x) * G::VW;
+        if (VEC)
+            v[i] = (e0 < p.V) ? ld_stream16(row + e0) : Vec16<T>::neg_inf();
+        else
+            v[i] = (e0 < p.V) ? Vec16<T>::load_scalar(row, e0, p.V) : Vec16<T>::neg_inf();
     }
-    // last row of the sequence decides it
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
-        s_last = (atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1));
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) p.seq_ticket[rr.b] = 0u;
-    decide_sequence<T>(p, rr.b);
+    segment_compute<T, MODE, NT>(p, [&](int i) { return v[i]; }, seg, r, (int)threadIdx.x,
+                                 [] { csync(); }, s_redf, s_redd);
 }
 
+// ------------------------------------------------------------------------- //
+// k_stream: persistent streaming kernel for rows that start on a 16-byte      //
+// boundary.  One producer thread issues bulk (TMA) copies of its work items   //
+// (row slot, segment), item = blockIdx.x + i * gridDim.x, into an NSTAGE ring //
+// of SEG_BYTES completing on mbarriers; NS stream threads compute each        //
+// segment's chunk-max keys or (max, sum) from shared memory.                 //
+// ------------------------------------------------------------------------- //
+struct Ring {
+    uint64_t full[NSTAGE];
+    uint64_t empty[NSTAGE];
+    int item[NSTAGE];
+};
+constexpr int STREAM_SMEM = NSTAGE * SEG_BYTES;
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
+{
+    extern __shared__ __align__(128) unsigned char smem_ring[];  // NSTAGE x SEG_BYTES
+    __shared__ Ring ring;
+    __shared__ float s_redf[NS / 32 + 1];
+    __shared__ double s_redd[NS / 32 + 1];
+    using G = SegGeom<T, NS>;
+    const int tid = threadIdx.x;
+    // the merge kernel that follows may be scheduled as this grid drains; it
+    // waits for this grid's completion before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();  // the only barrier over all STREAM_THREADS threads
+    const int64_t total_items = (int64_t)p.B * p.rps * p.nseg;
+    const int64_t row_bytes = (int64_t)p.V * (int64_t)sizeof(T);
+
+    if (tid >= NS) {
+        // ---------------- producer
+        if (tid != NS) return;
+        int k = 0;
+        bool failed = false;
+        for (int64_t item = blockIdx.x;; item += gridDim.x) {
+            if (item >= total_items) {
+                item = -1;
+            } else {
+                const int r = (int)(item / p.nseg), seg = (int)(item - (int64_t)r * p.nseg);
+                const RowRef rr = row_ref(p, r);
+                if (!rr.valid) continue;
+                if (rr.is_draft && p.draft_kind == 1) continue;
+            }
+            const int s = k % NSTAGE;
+            if (k >= NSTAGE && !mbar_wait(&ring.empty[s], ((k / NSTAGE) - 1) & 1)) {
+                atomicOr(p.err, 1u);
+                failed = true;
+                break;
+            }
+            ring.item[s] = (int)item;
+            if (item < 0) {
+                mbar_arrive(&ring.full[s]);  // the end-of-work sentinel
+                break;
+            }
+            const int r = (int)(item / p.nseg), seg = (int)(item - (int64_t)r * p.nseg);
+            const RowRef rr = row_ref(p, r);
+            const char* src = (const char*)(rr.is_draft ? p.draft : p.target) +
+                              row_elem_offset(p, rr) * (int64_t)sizeof(T) + (int64_t)seg * SEG_BYTES;
+            const uint32_t bytes =
+                (uint32_t)min((int64_t)SEG_BYTES, row_bytes - (int64_t)seg * SEG_BYTES);
+            mbar_arrive_expect_tx(&ring.full[s], bytes);
+            tma_load_1d(smem_ring + (size_t)s * SEG_BYTES, src, bytes, &ring.full[s]);
+            ++k;
+        }
+        if (failed) {
+            // wait (bounded) for the copies still in flight before leaving
+            for (int q = (k > NSTAGE ? k - NSTAGE : 0); q < k; ++q)
+                mbar_wait(&ring.full[q % NSTAGE], (q / NSTAGE) & 1);
+        }
+        return;
+    }
+
+    // ---------------- stream threads
+    for (int k = 0;; ++k) {
+        const int s = k % NSTAGE;
+        if (!mbar_wait(&ring.full[s], (k / NSTAGE) & 1)) {
+            atomicOr(p.err, 2u);
+            break;
+        }
+        const int item = ring.item[s];
+        if (item < 0) break;
+        const int r = item / p.nseg, seg = item - r * p.nseg;
+        const uint4* sv4 = reinterpret_cast<const uint4*>(smem_ring + (size_t)s * SEG_BYTES);
+        const int64_t base = (int64_t)seg * G::SEG;
+        segment_compute<T, MODE, NS>(
+            p,
+            [&](int i) {
+                const int64_t e0 = base + ((int64_t)i * NS + tid) * G::VW;
+                return e0 < p.V ? sv4[i * NS + tid] : Vec16<T>::neg_inf();
+            },
+            seg, r, tid, [] { ssync(); }, s_redf, s_redd);
+        ssync();  // every stream thread is done with the stage
+        if (tid == 0) mbar_arrive(&ring.empty[s]);
+    }
+}
+
+// ------------------------------------------------------------------------- //
+// k_merge: one CTA per row slot, after the whole stream: merge the row, then  //
+// the sequence ticket and the decision (verify) or the draft-row sample.     //
+// ------------------------------------------------------------------------- //
+template <typename T>
+__global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
+{
+    extern __shared__ __align__(16) unsigned char smem_scratch[];  // SCRATCH_BYTES
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream grid has completed
+    const int r = blockIdx.x;
+    const RowRef rr = row_ref(p, r);
+    if (!rr.valid) {
+        if (threadIdx.x == 0) report_skipped_row(p, rr);
+        return;
+    }
+    if (rr.is_draft && p.draft_kind == 1) return;  // probabilities: read only where needed
+    const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
+    finish_row<T>(p, r, rr, row, smem_scratch);
+}
+
+}  // namespace sv
+
+#include "sv_warp.cuh"
+
+namespace sv {
+
+// ------------------------------------------------------------------------- //
+// launchers                                                                 //
+// ------------------------------------------------------------------------- //
 template <typename T, bool VEC, int MODE>
 static cudaError_t launch_rows_t(const Params& p, cudaStream_t s)
 {
-    const int64_t rows = (int64_t)p.B * p.rps;
-    const int64_t grid = rows * p.nseg;
+    const int64_t grid = (int64_t)p.B * p.rps * p.nseg;
     if (grid <= 0) return cudaSuccess;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_rows<T, VEC, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ROWS_SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    k_rows<T, VEC, MODE><<<(unsigned)grid, NT, ROWS_SMEM, s>>>(p);
+    k_rows<T, VEC, MODE><<<(unsigned)grid, NT, SCRATCH_BYTES, s>>>(p);
     return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+static cudaError_t launch_stream_t(const Params& p, int ctas, cudaStream_t s)
+{
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_stream<T, MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    k_stream<T, MODE><<<ctas, STREAM_THREADS, STREAM_SMEM, s>>>(p);
+    return cudaGetLastError();
+}
+
+// a grid launched as a programmatic dependent of the previous one on the stream
+template <typename K>
+static cudaError_t launch_dependent(K kernel, const Params& p, unsigned grid, unsigned block,
+                                    int smem, cudaStream_t s)
+{
+    if (grid == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_merge_t(const Params& p, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)p.B * p.rps;
+    return launch_dependent(k_merge<T>, p, (unsigned)rows, NT, SCRATCH_BYTES, s);
+}
+
+template <typename T>
+static cudaError_t launch_merge_warp_t(const Params& p, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)p.B * p.rps;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e0 = cudaFuncSetAttribute(k_merge_warp<T>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, WM_SMEM);
+        if (e0 != cudaSuccess) return e0;
+        attr = true;
+    }
+    cudaError_t e = launch_dependent(k_merge_warp<T>, p,
+                                     (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
+                                     WM_WARPS * 32, WM_SMEM, s);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
 }
 
 cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s)
@@ -982,6 +1406,27 @@ cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s)
                           : launch_rows_t<float, true, SEG_SUM>(p, s);
     return chunk ? launch_rows_t<float, false, SEG_CHUNK>(p, s)
                  : launch_rows_t<float, false, SEG_SUM>(p, s);
+}
+
+cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_t s)
+{
+    if ((int64_t)p.B * p.rps * p.nseg <= 0) return cudaSuccess;
+    const bool chunk = p.seg_mode == SEG_CHUNK;
+    if (dtype == 1)
+        return chunk ? launch_stream_t<__nv_bfloat16, SEG_CHUNK>(p, ctas, s)
+                     : launch_stream_t<__nv_bfloat16, SEG_SUM>(p, ctas, s);
+    return chunk ? launch_stream_t<float, SEG_CHUNK>(p, ctas, s)
+                 : launch_stream_t<float, SEG_SUM>(p, ctas, s);
+}
+
+cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s)
+{
+    return dtype == 1 ? launch_merge_t<__nv_bfloat16>(p, s) : launch_merge_t<float>(p, s);
+}
+
+cudaError_t launch_merge_warp(const Params& p, int dtype, cudaStream_t s)
+{
+    return dtype == 1 ? launch_merge_warp_t<__nv_bfloat16>(p, s) : launch_merge_warp_t<float>(p, s);
 }
 
 }  // namespace sv

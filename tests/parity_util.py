@@ -94,14 +94,18 @@ def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL):
         np.testing.assert_array_equal(g["tokens"][b], o["tokens"][b], err_msg=f"sequence {b}")
         if st_o in (O.ROW_OK, O.ROW_ZERO_RESIDUAL):
             if "p_t_at_draft" in g:
+                # a row whose nucleus boundary lies inside the window may keep one
+                # boundary token more or less: its probabilities are not compared
+                sure_t = o["topp_margin_t"][b, :kb + 1] >= delta
+                sure = sure_t[:kb] & (o["topp_margin_d"][b, :kb] >= delta)
                 for name in ("p_t_at_draft", "p_d_at_draft"):
-                    np.testing.assert_allclose(g[name][b, :kb], o[name][b, :kb],
+                    np.testing.assert_allclose(g[name][b, :kb][sure], o[name][b, :kb][sure],
                                                rtol=prob_rtol, atol=PROB_ATOL,
                                                err_msg=f"{name} sequence {b}")
                     assert np.all(np.isnan(g[name][b, kb:]))
-                np.testing.assert_allclose(g["target_lse"][b, :kb + 1],
-                                           o["target_lse"][b, :kb + 1], rtol=0, atol=LSE_ATOL,
-                                           err_msg=f"lse sequence {b}")
+                np.testing.assert_allclose(g["target_lse"][b, :kb + 1][sure_t],
+                                           o["target_lse"][b, :kb + 1][sure_t], rtol=0,
+                                           atol=LSE_ATOL, err_msg=f"lse sequence {b}")
                 np.testing.assert_allclose(g["residual_mass"][b], o["residual_mass"][b],
                                            rtol=prob_rtol, atol=1e-7,
                                            err_msg=f"residual mass sequence {b}")
