@@ -151,6 +151,34 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
                               int32_t batch, int32_t k_max, const spec_sampling* s,
                               int32_t* draft_tokens, float* draft_probs, void* stream);
 
+/* The verify step for callers that cannot allocate device memory: a plugin
+ * or operator interface that is handed only a stream at enqueue time, a
+ * serving loop whose memory is a fixed arena owned by someone else, or code
+ * that must not trigger the implicit device synchronisation an allocation can
+ * cause.  The pages have no counterpart of this call: it is a deployment
+ * variant of spec_verify_run.
+ *
+ * It takes no handle and allocates nothing.  Its workspace is one static
+ * device array of SPEC_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * Inputs, outputs and their meaning are those of spec_verify_run; cfg gives
+ * the device, vocabulary, kinds and dtypes (its max_batch / max_k are not
+ * used: the sizes come from `in`).
+ *  - The first call on a device looks up the array's device address on that
+ *    device (once); make that first call before any stream capture begins.
+ *  - Sizes whose workspace would not fit the array return
+ *    SPEC_ERR_INVALID_ARG and launch nothing.  At V = 128256 and bf16 about
+ *    1100 row slots fit (B * (2 K_max + 1), e.g. B = 64 with K_max = 8); the
+ *    workspace per row slot is about 12.5 KB plus 4 bytes per 64 tokens.
+ *  - Every call shares the one array and each call reuses the last call's
+ *    contents (the counters that must start at zero are cleared on the
+ *    stream first), so calls that overlap on the GPU race: issue them on one
+ *    stream, or serialise them. */
+#define SPEC_NOALLOC_SCRATCH_BYTES (16u << 20)
+spec_status spec_verify_run_noalloc(const spec_verify_config* cfg, const spec_verify_inputs* in,
+                                    const spec_sampling* s, const spec_verify_outputs* out,
+                                    void* stream);
+
 /* Free the handle and its workspace (synchronises its device first). */
 spec_status spec_verify_destroy(spec_verify_t h);
 

@@ -27,7 +27,8 @@ SPEC_ROW_OK, SPEC_ROW_BAD_TOKEN, SPEC_ROW_BAD_K, SPEC_ROW_NONFINITE, \
 
 # every function the header declares (checked by the tests)
 ABI_FUNCTIONS = ("spec_verify_create", "spec_verify_run", "spec_draft_sample",
-                 "spec_verify_destroy", "spec_verify_status_string")
+                 "spec_verify_destroy", "spec_verify_status_string", "spec_verify_run_noalloc")
+SPEC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class spec_verify_config(C.Structure):
@@ -88,6 +89,10 @@ def load_library(path: str | None = None) -> C.CDLL:
     L.spec_verify_destroy.restype = C.c_int
     L.spec_verify_status_string.argtypes = [C.c_int]
     L.spec_verify_status_string.restype = C.c_char_p
+    L.spec_verify_run_noalloc.argtypes = [C.POINTER(spec_verify_config), C.POINTER(spec_verify_inputs),
+                                          C.POINTER(spec_sampling), C.POINTER(spec_verify_outputs),
+                                          C.c_void_p]
+    L.spec_verify_run_noalloc.restype = C.c_int
     if path is None:
         _lib = L
     return L
@@ -126,6 +131,16 @@ def spec_draft_sample(h, draft: int, k_per_row: int | None, batch: int, k_max: i
                                             C.c_void_p(draft_tokens),
                                             C.c_void_p(draft_probs or 0), C.c_void_p(stream)),
            "spec_draft_sample")
+
+
+def spec_verify_run_noalloc(cfg: spec_verify_config, inputs: spec_verify_inputs,
+                            sampling: spec_sampling, outputs: spec_verify_outputs,
+                            stream: int = 0) -> None:
+    """The verify step with the library's static workspace: no handle, no
+    allocation (for callers that cannot allocate device memory)."""
+    _check(load_library().spec_verify_run_noalloc(C.byref(cfg), C.byref(inputs), C.byref(sampling),
+                                                  C.byref(outputs), C.c_void_p(stream)),
+           "spec_verify_run_noalloc")
 
 
 def spec_verify_destroy(h) -> None:

@@ -345,3 +345,113 @@ spec_status spec_verify_destroy(spec_verify_t h)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------- //
+// Workspace laid over caller-provided device memory (used by the entry point  //
+// that allocates nothing, sv_noalloc.cu).  Same layout rules as create.       //
+// ------------------------------------------------------------------------- //
+namespace {
+
+// fills h (workspace pointers into ws, when ws is not NULL) for a run of
+// `batch` x `k_max`; returns the bytes needed, or 0 for invalid arguments
+size_t layout_over(spec_verify* h, const spec_verify_config* cfg, int32_t batch, int32_t k_max,
+                   void* ws)
+{
+    if (!cfg || batch < 0 || k_max < 0 || k_max > 255 || cfg->vocab < 1) return 0;
+    if (cfg->target_dtype != SPEC_F32 && cfg->target_dtype != SPEC_BF16) return 0;
+    if (cfg->draft_kind == SPEC_DRAFT_LOGITS) {
+        if (cfg->draft_dtype != cfg->target_dtype) return 0;
+    } else if (cfg->draft_kind == SPEC_DRAFT_PROBS) {
+        if (cfg->draft_dtype != SPEC_F32) return 0;
+    } else {
+        return 0;
+    }
+    if (cfg->target_kind != SPEC_TARGET_LOGITS) return 0;
+    if ((int64_t)cfg->vocab > (int64_t)NT * SAMPLE_SEG) return 0;
+    const int64_t mb = batch > 0 ? batch : 1;
+    const int64_t V = cfg->vocab;
+    h->cfg = *cfg;
+    h->cfg.max_batch = (int32_t)mb;
+    h->cfg.max_k = k_max;
+    h->rows_cap = mb * (2 * (int64_t)k_max + 1);
+    h->jobs_cap = mb * (k_max > 0 ? k_max : 1);
+    int dts[2] = {cfg->target_dtype, cfg->draft_dtype};
+    h->nseg_cap = 1;
+    h->nchunk_cap = 1;
+    for (int dt : dts) {
+        h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, seg_elems(dt)));
+        h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
+    }
+    h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
+    h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
+    if (h->rows_cap * h->nseg_cap >= (int64_t)INT32_MAX) return 0;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) & ~(size_t)255;
+        return at;
+    };
+    const size_t o_seg = take(sizeof(SegStat) * h->rows_cap * h->nseg_cap);
+    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->chunk_stride);
+    const size_t o_rstat = take(sizeof(RowStat) * h->rows_cap);
+    const size_t o_kid = take(sizeof(int32_t) * h->rows_cap * KCAP);
+    const size_t o_kl = take(sizeof(float) * h->rows_cap * KCAP);
+    const size_t o_rt = take(sizeof(unsigned) * h->rows_cap);
+    const size_t o_st = take(sizeof(unsigned) * mb);
+    const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
+    const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
+    const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
+    const size_t o_grab = take(sizeof(unsigned long long));
+    const size_t o_done = take(sizeof(unsigned));
+    const size_t o_err = take(sizeof(unsigned));
+    h->ws_bytes = off;
+    if (ws) {
+        char* b = (char*)ws;
+        h->ws = ws;
+        h->seg = (SegStat*)(b + o_seg);
+        h->chunk = (uint16_t*)(b + o_chunk);
+        h->rstat = (RowStat*)(b + o_rstat);
+        h->kept_id = (int32_t*)(b + o_kid);
+        h->kept_l = (float*)(b + o_kl);
+        h->row_ticket = (unsigned*)(b + o_rt);
+        h->seq_ticket = (unsigned*)(b + o_st);
+        h->jobs = (Job*)(b + o_jobs);
+        h->job_seg = (unsigned long long*)(b + o_jseg);
+        h->job_ticket = (unsigned*)(b + o_jt);
+        h->grab = (unsigned long long*)(b + o_grab);
+        h->done = (unsigned*)(b + o_done);
+        h->err = (unsigned*)(b + o_err);
+    }
+    return off;
+}
+
+}  // namespace
+
+// bytes of workspace a run of these sizes needs (0: invalid arguments)
+size_t sv_noalloc_bytes(const spec_verify_config* cfg, int32_t batch, int32_t k_max)
+{
+    spec_verify h;
+    return layout_over(&h, cfg, batch, k_max, nullptr);
+}
+
+// spec_verify_run over a workspace the caller provides (ws_bytes of device
+// memory on cfg->device, which must be current); allocates nothing
+spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_verify_config* cfg,
+                           const spec_verify_inputs* in, const spec_sampling* s,
+                           const spec_verify_outputs* out, void* stream)
+{
+    if (!ws || !in) return SPEC_ERR_INVALID_ARG;
+    spec_verify h;
+    const size_t need = layout_over(&h, cfg, in->batch, in->k_max, ws);
+    if (need == 0 || need > ws_bytes) return SPEC_ERR_INVALID_ARG;
+    h.num_sms = num_sms;
+    // the counters the kernels expect at zero (the array keeps the last call's contents)
+    cudaStream_t cs = (cudaStream_t)stream;
+    const size_t tickets = sizeof(unsigned) * (size_t)h.rows_cap;
+    if (cudaMemsetAsync(h.row_ticket, 0, tickets, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.seq_ticket, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.job_ticket, 0, sizeof(unsigned) * (size_t)h.jobs_cap, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.grab, 0, 256 * 3, cs) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return spec_verify_run(&h, in, s, out, stream);
+}
