@@ -35,6 +35,9 @@ struct spec_verify {
     unsigned long long* grab;
     unsigned* done;
     unsigned* err;
+    unsigned long long* cand_rows;  // NULL: this workspace has no candidate arrays
+    unsigned* rowctl;
+    unsigned* seq_done;
 };
 
 namespace {
@@ -97,6 +100,72 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.grab = h->grab;
     p.done = h->done;
     p.err = h->err;
+    p.rowctl = h->rowctl;
+    p.cand_rows = h->cand_rows;
+    p.seq_done = h->seq_done;
+}
+
+// one workspace: 256-byte aligned sub-buffers for max_batch x max_k x vocab;
+// candidate blocks only when with_cand.  Fills h's pointers when base is not
+// NULL; returns the bytes needed.
+size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
+{
+    const spec_verify_config* cfg = &h->cfg;
+    const int64_t V = cfg->vocab;
+    h->rows_cap = (int64_t)cfg->max_batch * (2 * (int64_t)cfg->max_k + 1);
+    h->jobs_cap = (int64_t)cfg->max_batch * (cfg->max_k > 0 ? cfg->max_k : 1);
+    int dts[2] = {cfg->target_dtype, cfg->draft_dtype};
+    h->nseg_cap = 1;
+    h->nchunk_cap = 1;
+    for (int dt : dts) {
+        h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, seg_elems(dt)));
+        h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
+    }
+    h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
+    h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) & ~(size_t)255;
+        return at;
+    };
+    const size_t o_seg = take(sizeof(SegStat) * h->rows_cap * h->nseg_cap);
+    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->chunk_stride);
+    const size_t o_rstat = take(sizeof(RowStat) * h->rows_cap);
+    const size_t o_kid = take(sizeof(int32_t) * h->rows_cap * KCAP);
+    const size_t o_kl = take(sizeof(float) * h->rows_cap * KCAP);
+    const size_t o_rt = take(sizeof(unsigned) * h->rows_cap);
+    const size_t o_st = take(sizeof(unsigned) * cfg->max_batch);
+    const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
+    const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
+    const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
+    const size_t o_grab = take(sizeof(unsigned long long));
+    const size_t o_done = take(sizeof(unsigned));
+    const size_t o_err = take(sizeof(unsigned));
+    const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
+    const size_t o_ctl = take(sizeof(unsigned) * 4 * h->rows_cap);
+    const size_t o_cand = with_cand ? take(sizeof(unsigned long long) * RCAP_ROW * h->rows_cap) : 0;
+    if (base) {
+        char* b = (char*)base;
+        h->ws = base;
+        h->seg = (SegStat*)(b + o_seg);
+        h->chunk = (uint16_t*)(b + o_chunk);
+        h->rstat = (RowStat*)(b + o_rstat);
+        h->kept_id = (int32_t*)(b + o_kid);
+        h->kept_l = (float*)(b + o_kl);
+        h->row_ticket = (unsigned*)(b + o_rt);
+        h->seq_ticket = (unsigned*)(b + o_st);
+        h->jobs = (Job*)(b + o_jobs);
+        h->job_seg = (unsigned long long*)(b + o_jseg);
+        h->job_ticket = (unsigned*)(b + o_jt);
+        h->grab = (unsigned long long*)(b + o_grab);
+        h->done = (unsigned*)(b + o_done);
+        h->err = (unsigned*)(b + o_err);
+        h->seq_done = (unsigned*)(b + o_sd);
+        h->rowctl = (unsigned*)(b + o_ctl);
+        h->cand_rows = with_cand ? (unsigned long long*)(b + o_cand) : nullptr;
+    }
+    return off;
 }
 
 // stage 1: stream every row (the persistent bulk-copy kernel when every row
@@ -106,8 +175,9 @@ void fill_workspace(const spec_verify* h, Params& p)
 cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool vec,
                           cudaStream_t s)
 {
-    cudaError_t e = vec ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
-                        : launch_rows(p, dtype, false, s);
+    cudaError_t e = p.cand ? launch_stream_cand(p, dtype, h->num_sms, s)
+                  : vec    ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
+                           : launch_rows(p, dtype, false, s);
     if (e != cudaSuccess) return e;
     return warp_merge_ok(p) ? launch_merge_warp(p, dtype, s) : launch_merge(p, dtype, s);
 }
@@ -171,74 +241,30 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
     spec_verify* h = new (std::nothrow) spec_verify();
     if (!h) return SPEC_ERR_OOM;
     h->cfg = *cfg;
-    const int64_t V = cfg->vocab;
-    h->rows_cap = (int64_t)cfg->max_batch * (2 * (int64_t)cfg->max_k + 1);
-    h->jobs_cap = (int64_t)cfg->max_batch * (cfg->max_k > 0 ? cfg->max_k : 1);
-    int dts[2] = {cfg->target_dtype, cfg->draft_dtype};
-    h->nseg_cap = 1;
-    h->nchunk_cap = 1;
-    for (int dt : dts) {
-        h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, seg_elems(dt)));
-        h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
-    }
-    h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
-    h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
     if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device) !=
         cudaSuccess) {
         delete h;
         return SPEC_ERR_CUDA;
     }
+    layout_workspace(h, true, nullptr);
     // stage-1 work items (row slot, segment) are counted in 32-bit ints
     if (h->rows_cap * h->nseg_cap >= (int64_t)INT32_MAX) {
         delete h;
         return SPEC_ERR_INVALID_ARG;
     }
-
-    // one allocation, 256-byte aligned sub-buffers
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        const size_t at = off;
-        off += (bytes + 255) & ~(size_t)255;
-        return at;
-    };
-    const size_t o_seg = take(sizeof(SegStat) * h->rows_cap * h->nseg_cap);
-    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->chunk_stride);
-    const size_t o_rstat = take(sizeof(RowStat) * h->rows_cap);
-    const size_t o_kid = take(sizeof(int32_t) * h->rows_cap * KCAP);
-    const size_t o_kl = take(sizeof(float) * h->rows_cap * KCAP);
-    const size_t o_rt = take(sizeof(unsigned) * h->rows_cap);
-    const size_t o_st = take(sizeof(unsigned) * cfg->max_batch);
-    const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
-    const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
-    const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
-    const size_t o_grab = take(sizeof(unsigned long long));
-    const size_t o_done = take(sizeof(unsigned));
-    const size_t o_err = take(sizeof(unsigned));
-    h->ws_bytes = off;
-    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+    h->ws_bytes = layout_workspace(h, true, nullptr);
+    void* base = nullptr;
+    if (cudaMalloc(&base, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return SPEC_ERR_OOM;
     }
-    if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
-        cudaFree(h->ws);
+    if (cudaMemset(base, 0, h->ws_bytes) != cudaSuccess) {
+        cudaFree(base);
         delete h;
         return SPEC_ERR_CUDA;
     }
-    char* b = (char*)h->ws;
-    h->seg = (SegStat*)(b + o_seg);
-    h->chunk = (uint16_t*)(b + o_chunk);
-    h->rstat = (RowStat*)(b + o_rstat);
-    h->kept_id = (int32_t*)(b + o_kid);
-    h->kept_l = (float*)(b + o_kl);
-    h->row_ticket = (unsigned*)(b + o_rt);
-    h->seq_ticket = (unsigned*)(b + o_st);
-    h->jobs = (Job*)(b + o_jobs);
-    h->job_seg = (unsigned long long*)(b + o_jseg);
-    h->job_ticket = (unsigned*)(b + o_jt);
-    h->grab = (unsigned long long*)(b + o_grab);
-    h->done = (unsigned*)(b + o_done);
-    h->err = (unsigned*)(b + o_err);
+    layout_workspace(h, true, base);
     *out = h;
     return SPEC_OK;
 }
@@ -281,6 +307,10 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     choose_seg_mode(p, dtype);
     const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(in->target) &&
                      (cfg.draft_kind == SPEC_DRAFT_PROBS || aligned16(in->draft));
+    // top-k rows: candidates written while each segment is in shared memory
+    p.npiece = (int)cdiv((int64_t)p.V * elem_size(dtype), CS_PIECE);
+    p.cand = vec && h->cand_rows && p.seg_mode == SEG_CHUNK && warp_merge_ok(p) &&
+             p.top_k >= 1 && p.top_k <= CAND_TOPK_MAX;
 
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
@@ -355,7 +385,7 @@ namespace {
 // fills h (workspace pointers into ws, when ws is not NULL) for a run of
 // `batch` x `k_max`; returns the bytes needed, or 0 for invalid arguments
 size_t layout_over(spec_verify* h, const spec_verify_config* cfg, int32_t batch, int32_t k_max,
-                   void* ws)
+                   void* ws, size_t ws_bytes)
 {
     if (!cfg || batch < 0 || k_max < 0 || k_max > 255 || cfg->vocab < 1) return 0;
     if (cfg->target_dtype != SPEC_F32 && cfg->target_dtype != SPEC_BF16) return 0;
@@ -369,59 +399,16 @@ size_t layout_over(spec_verify* h, const spec_verify_config* cfg, int32_t batch,
     if (cfg->target_kind != SPEC_TARGET_LOGITS) return 0;
     if ((int64_t)cfg->vocab > (int64_t)NT * SAMPLE_SEG) return 0;
     const int64_t mb = batch > 0 ? batch : 1;
-    const int64_t V = cfg->vocab;
     h->cfg = *cfg;
     h->cfg.max_batch = (int32_t)mb;
     h->cfg.max_k = k_max;
-    h->rows_cap = mb * (2 * (int64_t)k_max + 1);
-    h->jobs_cap = mb * (k_max > 0 ? k_max : 1);
-    int dts[2] = {cfg->target_dtype, cfg->draft_dtype};
-    h->nseg_cap = 1;
-    h->nchunk_cap = 1;
-    for (int dt : dts) {
-        h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, seg_elems(dt)));
-        h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
-    }
-    h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
-    h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
+    const size_t need = layout_workspace(h, false, nullptr);
     if (h->rows_cap * h->nseg_cap >= (int64_t)INT32_MAX) return 0;
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        const size_t at = off;
-        off += (bytes + 255) & ~(size_t)255;
-        return at;
-    };
-    const size_t o_seg = take(sizeof(SegStat) * h->rows_cap * h->nseg_cap);
-    const size_t o_chunk = take(sizeof(uint16_t) * h->rows_cap * h->chunk_stride);
-    const size_t o_rstat = take(sizeof(RowStat) * h->rows_cap);
-    const size_t o_kid = take(sizeof(int32_t) * h->rows_cap * KCAP);
-    const size_t o_kl = take(sizeof(float) * h->rows_cap * KCAP);
-    const size_t o_rt = take(sizeof(unsigned) * h->rows_cap);
-    const size_t o_st = take(sizeof(unsigned) * mb);
-    const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
-    const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
-    const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
-    const size_t o_grab = take(sizeof(unsigned long long));
-    const size_t o_done = take(sizeof(unsigned));
-    const size_t o_err = take(sizeof(unsigned));
-    h->ws_bytes = off;
-    if (ws) {
-        char* b = (char*)ws;
-        h->ws = ws;
-        h->seg = (SegStat*)(b + o_seg);
-        h->chunk = (uint16_t*)(b + o_chunk);
-        h->rstat = (RowStat*)(b + o_rstat);
-        h->kept_id = (int32_t*)(b + o_kid);
-        h->kept_l = (float*)(b + o_kl);
-        h->row_ticket = (unsigned*)(b + o_rt);
-        h->seq_ticket = (unsigned*)(b + o_st);
-        h->jobs = (Job*)(b + o_jobs);
-        h->job_seg = (unsigned long long*)(b + o_jseg);
-        h->job_ticket = (unsigned*)(b + o_jt);
-        h->grab = (unsigned long long*)(b + o_grab);
-        h->done = (unsigned*)(b + o_done);
-        h->err = (unsigned*)(b + o_err);
-    }
+    // candidate blocks when they fit in what is left of the caller's memory
+    const size_t with_cand = layout_workspace(h, true, nullptr);
+    const bool cand = ws && with_cand <= ws_bytes;
+    const size_t off = cand ? with_cand : need;
+    if (ws) layout_workspace(h, cand, ws);
     return off;
 }
 
@@ -431,7 +418,7 @@ size_t layout_over(spec_verify* h, const spec_verify_config* cfg, int32_t batch,
 size_t sv_noalloc_bytes(const spec_verify_config* cfg, int32_t batch, int32_t k_max)
 {
     spec_verify h;
-    return layout_over(&h, cfg, batch, k_max, nullptr);
+    return layout_over(&h, cfg, batch, k_max, nullptr, 0);
 }
 
 // spec_verify_run over a workspace the caller provides (ws_bytes of device
@@ -442,7 +429,7 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
 {
     if (!ws || !in) return SPEC_ERR_INVALID_ARG;
     spec_verify h;
-    const size_t need = layout_over(&h, cfg, in->batch, in->k_max, ws);
+    const size_t need = layout_over(&h, cfg, in->batch, in->k_max, ws, ws_bytes);
     if (need == 0 || need > ws_bytes) return SPEC_ERR_INVALID_ARG;
     h.num_sms = num_sms;
     // the counters the kernels expect at zero (the array keeps the last call's contents)
@@ -451,7 +438,9 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
     if (cudaMemsetAsync(h.row_ticket, 0, tickets, cs) != cudaSuccess ||
         cudaMemsetAsync(h.seq_ticket, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h.job_ticket, 0, sizeof(unsigned) * (size_t)h.jobs_cap, cs) != cudaSuccess ||
-        cudaMemsetAsync(h.grab, 0, 256 * 3, cs) != cudaSuccess)
+        cudaMemsetAsync(h.grab, 0, 256 * 3, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.rowctl, 0, sizeof(unsigned) * 4 * (size_t)h.rows_cap, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return spec_verify_run(&h, in, s, out, stream);
 }

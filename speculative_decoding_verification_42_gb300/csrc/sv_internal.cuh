@@ -33,7 +33,7 @@ constexpr int NBINS = 1 << DIGIT_BITS;
 constexpr int SAMPLE_SEG = 4096;    // elements of one stage-2 segment
 constexpr int SAMPLE_EPT = SAMPLE_SEG / NT;
 constexpr int WALK_EPT = 16;        // contiguous elements per thread in ordered walks
-constexpr int SCRATCH_BYTES = 32768;  // shared scratch of a row merge / sequence decision
+constexpr int SCRATCH_BYTES = 40960;  // shared scratch of a row merge / sequence decision
 constexpr int NSTAGE = 4;           // ring stages of the streaming kernel
 constexpr int NS = 128;             // stream threads of the streaming kernel
 // streaming kernel layout: stream warps [0, NS), one producer warp [NS, NS + 32)
@@ -63,6 +63,9 @@ struct __align__(16) RowStat {
     int32_t n_kept;   // size of the kept set
     int32_t mode;     // RowMode
     int32_t flags;    // FLAG_NONFINITE
+    float px;         // warp merges: P(x) of the row at its drafted token x_j
+                      // (0 when x_j is not kept or out of range)
+    int32_t pad[3];
 };
 
 struct __align__(8) Job {
@@ -120,7 +123,25 @@ struct Params {
     unsigned long long* grab; // streaming kernel: next work item (reset by the last CTA)
     unsigned* done;           // streaming kernel: CTAs finished
     unsigned* err;            // bounded waits that ran out (0 = none)
+    // top-k candidates written while a piece of a row is in shared memory
+    int32_t cand;             // 1: the candidate stream kernel runs (top-k <= CAND_TOPK_MAX)
+    int32_t npiece;           // pieces (CS_PIECE bytes) per row
+    unsigned* rowctl;         // [rows, 4]: candidate count, threshold, largest chunk key, 0
+    unsigned long long* cand_rows;  // [rows, RCAP_ROW] candidates (order key << 32 | token id)
+    unsigned* seq_done;       // [B] sequences decided inside the merge grid
 };
+
+// ------------------------------------------------------------------------- //
+// top-k candidates.  While a piece of a row is in shared memory its warp     //
+// knows a lower bound tau of the row's k-th largest logit: the k-th largest  //
+// of logits it has seen in the row (16-byte word maxima; each is a logit of  //
+// the row, so at least k logits are >= tau).  Every logit >= tau is a        //
+// candidate, so the row's top-k is contained in its candidates.              //
+// ------------------------------------------------------------------------- //
+constexpr int CS_PIECE = 4096;      // bytes of one piece (32 chunks of 128 bytes)
+constexpr int CAND_TOPK_MAX = 128;  // largest top-k the candidate path serves
+constexpr int RCAP_ROW = 2048;      // candidates a row can hold
+enum : int { CTL_COUNT = 0, CTL_TAU = 1, CTL_MAXKEY = 2 };
 
 // ------------------------------------------------------------------------- //
 // order keys: unsigned keys whose order is the order of the float values,    //
@@ -376,13 +397,15 @@ __host__ __device__ __forceinline__ int next_pow2(int n)
 // records written by another CTA of the same launch are read through L2
 __device__ __forceinline__ RowStat load_rowstat(const RowStat* src)
 {
-    static_assert(sizeof(RowStat) == 32, "RowStat is two 16-byte words");
+    static_assert(sizeof(RowStat) == 48, "RowStat is three 16-byte words");
     const uint4 a = __ldcg(reinterpret_cast<const uint4*>(src));
     const uint4 b = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
+    const uint4 c = __ldcg(reinterpret_cast<const uint4*>(src) + 2);
     RowStat r;
     uint4* d = reinterpret_cast<uint4*>(&r);
     d[0] = a;
     d[1] = b;
+    d[2] = c;
     return r;
 }
 
@@ -514,6 +537,8 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 // launchers (defined in the .cu files)
 cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_t s);
+// the candidate stream kernel (one warp per CTA, as many as fit each SM)
+cudaError_t launch_stream_cand(const Params& p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);
 cudaError_t launch_merge_warp(const Params& p, int dtype, cudaStream_t s);
 // rows whose merge the warp kernel handles: fast top-k rows, or rows without knobs

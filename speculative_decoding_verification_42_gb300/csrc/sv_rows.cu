@@ -117,13 +117,45 @@ template <> struct ChunkMax<__nv_bfloat16> {
     static __device__ __forceinline__ P lane(uint4 w) { return mx(mx(w.x, w.y), mx(w.z, w.w)); }
     static __device__ __forceinline__ P shfl(P v, int o) { return mx(v, __shfl_xor_sync(0xffffffffu, v, o)); }
     static __device__ __forceinline__ float value(P v) { return fmax_nan(bf16_lo(v), bf16_hi(v)); }
+    // threshold operand of the packed compares: a float threshold whose order
+    // key has zero low bits compares like its upper 16 bits (a bf16) against
+    // bf16 values; t2 holds that bf16 twice
+    static __device__ __forceinline__ uint32_t thr2(float t)
+    {
+        const uint32_t h = __float_as_uint(t) >> 16;
+        return h | (h << 16);
+    }
+    static __device__ __forceinline__ uint32_t ge2(uint32_t a, uint32_t t2)
+    {
+        return __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                           *reinterpret_cast<const __nv_bfloat162*>(&t2));
+    }
+    // does either packed maximum reach the threshold?
+    static __device__ __forceinline__ bool any_ge(P v, float, uint32_t t2) { return ge2(v, t2) != 0u; }
+    // bit q set iff element q of the word reaches the threshold
+    static __device__ __forceinline__ uint32_t elem_mask(uint4 w, float, uint32_t t2)
+    {
+        const uint32_t m[4] = {ge2(w.x, t2), ge2(w.y, t2), ge2(w.z, t2), ge2(w.w, t2)};
+        uint32_t e = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e |= ((m[i] & 1u) | ((m[i] >> 15) & 2u)) << (2 * i);
+        return e;
+    }
 };
 
 template <> struct ChunkMax<float> {
     using P = float;
+    static __device__ __forceinline__ float mx(float a, float b) { return fmax_nan(a, b); }
     static __device__ __forceinline__ P lane(uint4 w) { return Vec16<float>::vmax(w); }
     static __device__ __forceinline__ P shfl(P v, int o) { return fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o)); }
     static __device__ __forceinline__ float value(P v) { return v; }
+    static __device__ __forceinline__ uint32_t thr2(float) { return 0u; }
+    static __device__ __forceinline__ bool any_ge(P v, float t, uint32_t) { return v >= t; }
+    static __device__ __forceinline__ uint32_t elem_mask(uint4 w, float t, uint32_t)
+    {
+        return (__uint_as_float(w.x) >= t ? 1u : 0u) | (__uint_as_float(w.y) >= t ? 2u : 0u) |
+               (__uint_as_float(w.z) >= t ? 4u : 0u) | (__uint_as_float(w.w) >= t ? 8u : 0u);
+    }
 };
 
 // ------------------------------------------------------------------------- //
@@ -1318,6 +1350,7 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 }  // namespace sv
 
 #include "sv_warp.cuh"
+#include "sv_cand.cuh"
 
 namespace sv {
 
@@ -1329,7 +1362,7 @@ static cudaError_t launch_rows_t(const Params& p, cudaStream_t s)
 {
     const int64_t grid = (int64_t)p.B * p.rps * p.nseg;
     if (grid <= 0) return cudaSuccess;
-    k_rows<T, VEC, MODE><<<(unsigned)grid, NT, SCRATCH_BYTES, s>>>(p);
+    k_rows<T, VEC, MODE><<<(unsigned)grid, NT, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -49,7 +49,7 @@ __device__ __forceinline__ void warp_sort_keys(const unsigned long long* src, un
                                                int n)
 {
     const int lane = threadIdx.x & 31;
-    if (n <= 64) {  // counting rank
+    if (n <= 128) {  // counting rank
         for (int i = lane; i < n; i += 32) {
             const unsigned long long x = src[i];
             int rk = 0;
@@ -65,15 +65,107 @@ __device__ __forceinline__ void warp_sort_keys(const unsigned long long* src, un
     warp_bitonic_u64(dst, n2);
 }
 
+// exclusive prefix sum over the warp; *total gets the sum of all lanes
+__device__ __forceinline__ int warp_excl_scan(int v, int* total)
+{
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if ((threadIdx.x & 31) >= o) x += y;
+    }
+    *total = __shfl_sync(0xffffffffu, x, 31);
+    return x - v;
+}
+
+// P(x) of a merged row, the same arithmetic the decisions use
+__device__ __forceinline__ float row_prob(const Params& p, float l, float M, double S)
+{
+    return (float)((double)exp2f((l - M) * p.c) / S);
+}
+
+// The n candidates in ws.cand (sort keys (~order key) << 32 | id, a superset
+// of the top-k) become the row's kept list: exact order (key descending, id
+// ascending), the first k, the top-p prefix, then the list in ascending id
+// written to the workspace with M, S and P(x) of the drafted token x (x < 0:
+// none).
+__device__ void warp_topk_tail(const Params& p, int r, WarpSmem& ws, int n, int x, RowStat& st)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const float c = p.c;
+    warp_sort_keys(ws.cand, ws.srt, n);
+    const int kk = min(p.top_k, n);
+    const float M = val_of(~(uint32_t)(ws.srt[0] >> 32));
+    float e_loc = 0.f;
+    for (int i = lane; i < kk; i += 32) e_loc += ex2_fast((val_of(~(uint32_t)(ws.srt[i] >> 32)) - M) * c);
+    double S = warp_sum_d((double)e_loc);
+    int nk = kk;
+    if (p.top_p < 1.0f) {
+        double pre = 0.0;
+        int stop = kk;
+        for (int b0 = 0; b0 < kk; b0 += 32) {
+            const int i = b0 + lane;
+            const double pv =
+                i < kk ? (double)ex2_fast((val_of(~(uint32_t)(ws.srt[i] >> 32)) - M) * c) / S : 0.0;
+            double y = pv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double t = __shfl_up_sync(FULL, y, o);
+                if (lane >= o) y += t;
+            }
+            const double before = pre + (y - pv);  // mass strictly before rank i
+            const unsigned drop = __ballot_sync(FULL, i < kk && !(before < (double)p.top_p));
+            if (drop) {
+                stop = b0 + __ffs(drop) - 1;
+                break;
+            }
+            pre += __shfl_sync(FULL, y, 31);
+        }
+        nk = stop;
+        float e2 = 0.f;
+        for (int i = lane; i < nk; i += 32) e2 += ex2_fast((val_of(~(uint32_t)(ws.srt[i] >> 32)) - M) * c);
+        S = warp_sum_d((double)e2);
+    }
+    // the kept list in ascending id
+    for (int i = lane; i < nk; i += 32) {
+        const unsigned long long v = ws.srt[i];
+        ws.cand[i] = ((unsigned long long)(uint32_t)v << 32) | (uint32_t)(~(uint32_t)(v >> 32));
+    }
+    __syncwarp();
+    warp_sort_keys(ws.cand, ws.srt, nk);
+    int32_t* kid = p.kept_id + (int64_t)r * KCAP;
+    float* kl = p.kept_l + (int64_t)r * KCAP;
+    float lx = 0.f;
+    bool found = false;
+    for (int i = lane; i < nk; i += 32) {
+        const unsigned long long v = ws.srt[i];
+        const int id = (int)(v >> 32);
+        const float l = val_of((uint32_t)v);
+        kid[i] = id;
+        kl[i] = l;
+        if (id == x) {
+            found = true;
+            lx = l;
+        }
+    }
+    const unsigned hit = __ballot_sync(FULL, found);
+    lx = __shfl_sync(FULL, lx, hit ? __ffs(hit) - 1 : 0);
+    st.M = M;
+    st.S = S;
+    st.n_kept = nk;
+    st.mode = MODE_LIST;
+    st.px = hit ? row_prob(p, lx, M, S) : 0.f;
+}
+
 // warp-level fast top-k (same result as fast_topk); false when the warp's
 // staging overflows
 template <typename T>
-__device__ bool warp_fast_topk(const Params& p, const T* row, int r, WarpSmem& ws, RowStat& st)
+__device__ bool warp_fast_topk(const Params& p, const T* row, int r, int x, WarpSmem& ws, RowStat& st)
 {
     const int lane = threadIdx.x & 31;
     const unsigned FULL = 0xffffffffu;
     const int V = p.V, k = p.top_k, nc = p.nchunk;
-    const float c = p.c;
     using G = SegGeom<T, NT>;
     if (nc > WM_KEYS || k > WM_CAND) return false;
 
@@ -202,60 +294,64 @@ __device__ bool warp_fast_topk(const Params& p, const T* row, int r, WarpSmem& w
         }
     }
     __syncwarp();
-    __syncwarp();
-    // exact order: key descending, then id ascending
-    warp_sort_keys(ws.cand, ws.srt, n);
-    const int kk = min(k, n);
-    const float M = val_of(~(uint32_t)(ws.srt[0] >> 32));
-    float e_loc = 0.f;
-    for (int i = lane; i < kk; i += 32) e_loc += ex2_fast((val_of(~(uint32_t)(ws.srt[i] >> 32)) - M) * c);
-    double S = warp_sum_d((double)e_loc);
-    int nk = kk;
-    if (p.top_p < 1.0f) {
-        double pre = 0.0;
-        int stop = kk;
-        for (int b0 = 0; b0 < kk; b0 += 32) {
-            const int i = b0 + lane;
-            const double pv =
-                i < kk ? (double)ex2_fast((val_of(~(uint32_t)(ws.srt[i] >> 32)) - M) * c) / S : 0.0;
-            double x = pv;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(FULL, x, o);
-                if (lane >= o) x += y;
-            }
-            const double before = pre + (x - pv);  // mass strictly before rank i
-            const unsigned drop = __ballot_sync(FULL, i < kk && !(before < (double)p.top_p));
-            if (drop) {
-                stop = b0 + __ffs(drop) - 1;
-                break;
-            }
-            pre += __shfl_sync(FULL, x, 31);
-        }
-        nk = stop;
-        float e2 = 0.f;
-        for (int i = lane; i < nk; i += 32) e2 += ex2_fast((val_of(~(uint32_t)(ws.srt[i] >> 32)) - M) * c);
-        S = warp_sum_d((double)e2);
-    }
-    // the kept list in ascending id
-    for (int i = lane; i < nk; i += 32) {
-        const unsigned long long x = ws.srt[i];
-        ws.cand[i] = ((unsigned long long)(uint32_t)x << 32) | (uint32_t)(~(uint32_t)(x >> 32));
-    }
-    __syncwarp();
-    warp_sort_keys(ws.cand, ws.srt, nk);
-    int32_t* kid = p.kept_id + (int64_t)r * KCAP;
-    float* kl = p.kept_l + (int64_t)r * KCAP;
-    for (int i = lane; i < nk; i += 32) {
-        const unsigned long long x = ws.srt[i];
-        kid[i] = (int32_t)(x >> 32);
-        kl[i] = val_of((uint32_t)x);
-    }
-    st.M = M;
-    st.S = S;
-    st.n_kept = nk;
-    st.mode = MODE_LIST;
+    warp_topk_tail(p, r, ws, n, x, st);
     return true;
+}
+
+// the top-k of row r from the candidates the stream kernel collected (a flat
+// array and the row's control words, reset here for the next launch): 1 when
+// st is final, 0 when the chunk-key path has to run instead (candidates were
+// lost, or more pass the row threshold than the warp stages)
+template <typename T>
+__device__ int warp_cand_topk(const Params& p, int r, int x, WarpSmem& ws, RowStat& st)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    unsigned* ctl = p.rowctl + (int64_t)r * 4;
+    const uint4 c4 = __ldcg(reinterpret_cast<const uint4*>(ctl));
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<uint4*>(ctl) = make_uint4(0, 0, 0, 0);
+    const uint32_t cnt = c4.x, tau = c4.y, maxkey = c4.z;
+    if (maxkey >= 0xFF80u || maxkey <= 0x007Fu) {  // NaN or +inf, or no finite logit
+        st.flags = FLAG_NONFINITE;
+        return 1;
+    }
+    if (cnt > (uint32_t)RCAP_ROW || cnt == 0u) return 0;
+    // the candidates, two per 16-byte load, eight loads in flight per lane;
+    // those at or above the row threshold are appended with ballots
+    const uint4* src = reinterpret_cast<const uint4*>(p.cand_rows + (int64_t)r * RCAP_ROW);
+    const int nw = (int)((cnt + 1u) / 2u);
+    int n = 0;
+#pragma unroll 1
+    for (int w0 = 0; w0 < nw; w0 += 32 * 8) {
+        uint4 w[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const int wi = w0 + g * 32 + lane;
+            w[g] = wi < nw ? __ldcg(src + wi) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const int wi = w0 + g * 32 + lane;
+            if (w0 + g * 32 >= nw) break;  // warp-uniform
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t key = h ? w[g].w : w[g].y;
+                const uint32_t id = h ? w[g].z : w[g].x;
+                const bool take = wi < nw && 2 * wi + h < (int)cnt && (key >> 16) >= tau;
+                const unsigned bal = __ballot_sync(FULL, take);
+                if (n + __popc(bal) > WM_CAND) return 0;
+                if (take)
+                    ws.cand[n + __popc(bal & ((1u << lane) - 1u))] =
+                        ((unsigned long long)(~key) << 32) | id;
+                n += __popc(bal);
+            }
+        }
+    }
+    __syncwarp();
+    if (n < 1) return 0;  // cannot happen for a finite row; the chunk path decides
+    warp_topk_tail(p, r, ws, n, x, st);
+    return 1;
 }
 
 // statistics over all tokens (no knobs) from the segment records, by one warp
@@ -284,13 +380,227 @@ __device__ __forceinline__ void warp_all_stats(const Params& p, int r, RowStat& 
 }
 
 // ------------------------------------------------------------------------- //
-// k_merge_warp: one warp per row slot (after the stream grid)                //
+// the decision of one sequence by one warp, inside the merge grid: every row //
+// record carries P(x_j), so the accept tests need no lookups; the emitted    //
+// token is drawn from the target's kept list (residual or bonus) by inverse  //
+// CDF in fixed point, or posted as a job for the full-row sampler.           //
+// ------------------------------------------------------------------------- //
+template <typename T>
+__device__ int warp_sample_list(const Params& p, int tr, const RowStat& ts, bool residual,
+                                const DraftRef& d, float u, WarpSmem& ws,
+                                unsigned long long* Zfix, bool* zero)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int n = ts.n_kept;  // <= WM_CAND in the warp path
+    int32_t* ti = reinterpret_cast<int32_t*>(ws.keys);
+    float* tv = reinterpret_cast<float*>(ws.keys) + WM_CAND;
+    int32_t* di = reinterpret_cast<int32_t*>(ws.keys) + 2 * WM_CAND;
+    float* dv = reinterpret_cast<float*>(ws.keys) + 3 * WM_CAND;
+    static_assert(4 * WM_CAND * 4 <= (int)sizeof(ws.keys), "two staged lists fit the key staging");
+    StagedList tl{ti, tv, n}, dl{di, dv, 0};
+    {
+        const int32_t* gi = p.kept_id + (int64_t)tr * KCAP;
+        const float* gv = p.kept_l + (int64_t)tr * KCAP;
+        for (int i = lane; i < n; i += 32) {
+            ti[i] = __ldcg(gi + i);
+            tv[i] = __ldcg(gv + i);
+        }
+        if (residual && d.kind == 0 && d.st.mode == MODE_LIST) {
+            dl.n = d.st.n_kept;
+            const int32_t* hi = p.kept_id + (int64_t)d.r * KCAP;
+            const float* hv = p.kept_l + (int64_t)d.r * KCAP;
+            for (int i = lane; i < dl.n; i += 32) {
+                di[i] = __ldcg(hi + i);
+                dv[i] = __ldcg(hv + i);
+            }
+        }
+        __syncwarp();
+    }
+    const float invSt = (float)(1.0 / ts.S);
+    const float invSd = (residual && d.kind == 0) ? (float)(1.0 / d.st.S) : 0.f;
+    const int ept = (n + 31) / 32;
+    const int i0 = lane * ept;
+    *zero = false;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const bool res = residual && attempt == 0;
+        unsigned long long part = 0;
+        for (int q = 0; q < ept; ++q) {
+            const int i = i0 + q;
+            if (i >= n) break;
+            part += list_r_fix<T>(p, ts, tl, i, res, d, dl, invSt, invSd);
+        }
+        unsigned long long incl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned long long Z = __shfl_sync(FULL, incl, 31);
+        const unsigned long long ex = incl - part;
+        if (attempt == 0) *Zfix = Z;
+        if (Z == 0ull) {
+            if (res) {
+                *zero = true;
+                continue;
+            }
+            return -1;
+        }
+        const unsigned long long t = cdf_target(u, Z);
+        int tok = -1;
+        if (ex <= t && t < ex + part) {
+            unsigned long long acc = ex;
+            for (int q = 0; q < ept; ++q) {
+                const int i = i0 + q;
+                if (i >= n) break;
+                acc += list_r_fix<T>(p, ts, tl, i, res, d, dl, invSt, invSd);
+                if (acc > t) {
+                    tok = tl.ids[i];
+                    break;
+                }
+            }
+        }
+        return __reduce_max_sync(FULL, tok);
+    }
+    return -1;
+}
+
+// true when the warp decided sequence b; false leaves it to the decision grid
+// (a row of it needs the block merge)
+template <typename T>
+__device__ bool warp_decide(const Params& p, int b, WarpSmem& ws)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int K = p.Kmax, V = p.V;
+    const int kb = seq_k(p, b);
+    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
+    const int64_t drow0 = (int64_t)b * K * V;
+    bool bad = false, nonf = false, block = false;
+    for (int i = lane; i < nrows; i += 32) {
+        const int r = i <= kb ? target_slot(p, b, i) : draft_slot(p, b, i - kb - 1);
+        const int fl = __ldcg(&p.rstat[r].flags);
+        nonf |= (fl & FLAG_NONFINITE) != 0;
+        // a kept list longer than the warp stages is sampled by the block code
+        block |= (fl & FLAG_BLOCK_MERGE) != 0 ||
+                 (__ldcg(&p.rstat[r].mode) == MODE_LIST && __ldcg(&p.rstat[r].n_kept) > WM_CAND);
+    }
+    if (__any_sync(FULL, block)) return false;
+    for (int j = lane; j < kb; j += 32) {
+        const int x = p.xin[(int64_t)b * K + j];
+        if (x < 0 || x >= V) {
+            bad = true;
+        } else if (p.draft_kind == 1) {
+            const float q = __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x);
+            if (!(q >= 0.f) || q == INFINITY) nonf = true;
+        }
+    }
+    bad = __any_sync(FULL, bad);
+    nonf = __any_sync(FULL, nonf);
+    if (bad || nonf) {
+        for (int j = lane; j <= K; j += 32) {
+            p.tokens[(int64_t)b * (K + 1) + j] = -1;
+            if (p.lse) p.lse[(int64_t)b * (K + 1) + j] = NAN;
+            if (j < K) {
+                if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
+                if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = NAN;
+            }
+        }
+        if (lane == 0) {
+            p.num_accepted[b] = -1;
+            if (p.row_status) p.row_status[b] = bad ? ROW_BAD_TOKEN : ROW_NONFINITE;
+            if (p.resid_mass) p.resid_mass[b] = NAN;
+            p.jobs[b].kind = JOB_NONE;
+        }
+        return true;
+    }
+    // accept tests, every slot; the first rejection is the smallest rejected j
+    int jstar = kb;
+    for (int j0 = 0; j0 < kb; j0 += 32) {
+        const int j = j0 + lane;
+        bool rej = false;
+        if (j < kb) {
+            const int x = p.xin[(int64_t)b * K + j];
+            const float pt = __ldcg(&p.rstat[target_slot(p, b, j)].px);
+            const float pd = p.draft_kind == 1
+                                 ? __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x)
+                                 : __ldcg(&p.rstat[draft_slot(p, b, j)].px);
+            const uint4 w = slot_words(p, b, j, 0u);
+            const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
+            rej = !((double)u24(w.x) < ratio);
+            if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = pt;
+            if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = pd;
+        }
+        const unsigned m = __ballot_sync(FULL, rej);
+        if (m && jstar == kb) jstar = j0 + __ffs(m) - 1;
+    }
+    for (int j = lane; j <= K; j += 32) {
+        if (p.lse) {
+            float v = NAN;
+            if (j <= kb) {
+                const RowStat* rs = p.rstat + target_slot(p, b, j);
+                v = (float)((double)__ldcg(&rs->M) / (double)p.T + log(__ldcg(&rs->S)));
+            }
+            p.lse[(int64_t)b * (K + 1) + j] = v;
+        }
+        if (j >= kb && j < K) {
+            if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
+            if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = NAN;
+        }
+        if (j != jstar) p.tokens[(int64_t)b * (K + 1) + j] = j < jstar ? p.xin[(int64_t)b * K + j] : -1;
+    }
+    const bool residual = jstar < kb;
+    const uint4 w = slot_words(p, b, jstar, 0u);
+    const float u = u24(w.y);
+    const int tr = target_slot(p, b, jstar);
+    const RowStat ts = load_rowstat(p.rstat + tr);
+    DraftRef d;
+    d.kind = p.draft_kind;
+    d.r = residual ? draft_slot(p, b, jstar) : -1;
+    if (residual && d.kind == 0) d.st = load_rowstat(p.rstat + d.r);
+    d.row = residual ? (const void*)((const char*)p.draft +
+                                     (drow0 + (int64_t)jstar * V) * (d.kind == 1 ? 4 : (int64_t)sizeof(T)))
+                     : nullptr;
+    if (ts.mode == MODE_LIST) {
+        unsigned long long Z;
+        bool zero;
+        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, ws, &Z, &zero);
+        if (lane == 0) {
+            p.tokens[(int64_t)b * (K + 1) + jstar] = tok;
+            p.num_accepted[b] = jstar;
+            if (p.row_status) p.row_status[b] = zero ? ROW_ZERO_RESIDUAL : ROW_OK;
+            if (p.resid_mass) p.resid_mass[b] = residual ? (float)from_fix56(Z) : 0.f;
+            p.jobs[b].kind = JOB_NONE;
+        }
+    } else if (lane == 0) {
+        p.tokens[(int64_t)b * (K + 1) + jstar] = -1;
+        p.num_accepted[b] = jstar;
+        if (p.row_status) p.row_status[b] = ROW_OK;
+        if (p.resid_mass && !residual) p.resid_mass[b] = 0.f;
+        Job jb;
+        jb.kind = residual ? JOB_RESIDUAL : JOB_ROW;
+        jb.trow = tr;
+        jb.drow = residual ? d.r : -1;
+        jb.out_idx = b * (K + 1) + jstar;
+        jb.b = b;
+        jb.u = u;
+        p.jobs[b] = jb;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------------- //
+// k_merge_warp: one warp per row slot (after the stream grid).  The last row //
+// of a sequence to finish (a ticket) decides the sequence.                   //
 // ------------------------------------------------------------------------- //
 template <typename T>
 __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
 {
     extern __shared__ __align__(16) unsigned char smem_w[];
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream grid has completed
+    // the decision grid may be scheduled now; it waits for this grid's end
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const unsigned FULL = 0xffffffffu;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * WM_WARPS + warp;
     if (r >= p.B * p.rps) return;
@@ -302,6 +612,12 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     if (rr.is_draft && p.draft_kind == 1) return;
     WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_w)[warp];
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
+    // the drafted token this row's P(x) is needed at (the bonus row has none)
+    int x = -1;
+    if (rr.j < rr.kb) {
+        x = p.xin[(int64_t)rr.b * p.Kmax + rr.j];
+        if (x < 0 || x >= p.V) x = -1;
+    }
     RowStat st;
     st.M = -INFINITY;
     st.kappa = 0;
@@ -310,26 +626,54 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     st.n_kept = p.V;
     st.mode = MODE_ALL;
     st.flags = 0;
+    st.px = 0.f;
+    st.pad[0] = st.pad[1] = st.pad[2] = 0;
     if (p.seg_mode == SEG_CHUNK) {
-        if (!warp_fast_topk<T>(p, row, r, ws, st)) st.flags |= FLAG_BLOCK_MERGE;
+        const int done = p.cand ? warp_cand_topk<T>(p, r, x, ws, st) : 0;
+        if (!done && !warp_fast_topk<T>(p, row, r, x, ws, st)) st.flags |= FLAG_BLOCK_MERGE;
     } else {
         warp_all_stats(p, r, st);
+        if (!st.flags && x >= 0) st.px = row_prob(p, Elem<T>::load_cg(row, x), st.M, st.S);
     }
     if (lane == 0) p.rstat[r] = st;
+    // sequence ticket: every lane's writes are fenced before lane 0 takes it
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+        const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
+        last = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
+        if (last) p.seq_ticket[rr.b] = 0u;
+    }
+    last = __shfl_sync(FULL, last, 0);
+    if (!last) return;
+    __threadfence();
+    if (warp_decide<T>(p, rr.b, ws)) {
+        __syncwarp();
+        if (lane == 0) p.seq_done[rr.b] = 1u;
+    }
 }
 
 // ------------------------------------------------------------------------- //
-// k_decide: one CTA per sequence: rows the warp merge flagged are merged by  //
-// the block code, then the sequence is decided                              //
+// k_decide: one CTA per sequence the merge grid did not decide: the rows the //
+// warp merge flagged are merged by the block code, then the sequence is      //
+// decided                                                                    //
 // ------------------------------------------------------------------------- //
 template <typename T>
 __global__ void __launch_bounds__(NT) k_decide(const Params p)
 {
     extern __shared__ __align__(16) unsigned char smem_scratch[];  // SCRATCH_BYTES
+    __shared__ int s_done;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the merge grid has completed
     const int b = blockIdx.x;
     const int kb = seq_k(p, b);
     if (!k_ok(p, kb)) return;  // reported by the merge grid
+    if (threadIdx.x == 0) {
+        s_done = (int)__ldcg(p.seq_done + b);
+        if (s_done) p.seq_done[b] = 0u;
+    }
+    csync();
+    if (s_done) return;
     const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
     // which rows the warps left to the block code (bitmask, one load round)
     __shared__ unsigned s_flagged[(2 * 255 + 1 + 31) / 32];

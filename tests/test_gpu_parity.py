@@ -79,6 +79,52 @@ def test_several_segments(orc, V, dtype, knobs):
     _check(orc, w)
 
 
+# ----------------------------------------------- top-k candidate stream --
+# Top-k rows (k <= 128, 16-byte rows) take the stream kernel that writes the
+# logits at or above a running top-k bound while each segment is in shared
+# memory.  Its warps own runs of consecutive segments, so the bound carries
+# across the segments of a row once a batch has more segments than the grid
+# has warps (these sizes do); a segment with fewer than k chunks uses its
+# 16-byte word maxima; an overflowing segment sends the row to the chunk path.
+@pytest.mark.parametrize("V,dtype,B,K,knobs", [
+    (128256, "bf16", 16, 8, dict(top_k=50, temperature=0.7)),
+    (128256, "f32", 8, 8, dict(top_k=50)),                  # last segment: 40 chunks < k
+    (100000, "bf16", 12, 6, dict(top_k=128, top_p=0.95)),   # largest k of the path
+    (65536, "bf16", 16, 4, dict(top_k=1, temperature=1.5)),
+    (40000, "f32", 24, 5, dict(top_k=7, temperature=0.5)),
+])
+def test_candidate_stream(orc, V, dtype, B, K, knobs):
+    w = make_workload(f"cand V={V}", B=B, K_max=K, V=V, dtype=dtype, target_std=3.0, peaks=20,
+                      peak_height=8.0, draft_noise_std=1.0, ragged_k=(0, K), seed=V + B,
+                      **knobs)
+    _check(orc, w)
+
+
+def test_candidate_stream_heavy_ties(orc):
+    """Logits rounded to integers: many logits tie at the bound, so some
+    segments overflow their candidate block and those rows take the chunk
+    path; ties keep the lowest ids either way."""
+    from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
+    w = make_workload("ties-int", B=8, K_max=4, V=50000, dtype="bf16", target_std=1.5,
+                      draft_noise_std=0.7, seed=41, top_k=60)
+    w.target = f32_to_bf16_bits(np.round(bf16_bits_to_f32(w.target)))
+    w.draft = f32_to_bf16_bits(np.round(bf16_bits_to_f32(w.draft)))
+    _check(orc, w)
+
+
+def test_candidate_stream_draft_probs(orc):
+    """Top-k target rows through the candidate stream, draft given as f32
+    probabilities (not streamed)."""
+    w = make_workload("cand-probs", B=10, K_max=5, V=40960, dtype="f32", ragged_k=(0, 5),
+                      seed=52, temperature=0.9, top_k=20)
+    q = np.empty_like(w.draft)
+    for b in range(w.B):
+        for j in range(w.K_max):
+            q[b, j] = orc.row_probs(w.draft[b, j], 0.9, 20)[0].astype(np.float32)
+    w.draft, w.draft_kind = q, "probs"
+    _check(orc, w)
+
+
 # ------------------------------------------------------ the five workloads --
 def test_config1_tiny(orc):
     _check(orc, make_config(1))
