@@ -337,8 +337,9 @@ __device__ int warp_cand_topk(const Params& p, int r, int x, WarpSmem& ws, RowSt
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t key = h ? w[g].w : w[g].y;
-                const uint32_t id = h ? w[g].z : w[g].x;
-                const bool take = wi < nw && 2 * wi + h < (int)cnt && (key >> 16) >= tau;
+                const uint32_t id = h ? w[g].z : w[g].x;  // ~0: an unused slot
+                const bool take = wi < nw && 2 * wi + h < (int)cnt && id < (uint32_t)p.V &&
+                                  (key >> 16) >= tau;
                 const unsigned bal = __ballot_sync(FULL, take);
                 if (n + __popc(bal) > WM_CAND) return 0;
                 if (take)
