@@ -1351,6 +1351,7 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 
 #include "sv_warp.cuh"
 #include "sv_cand.cuh"
+#include "sv_mcand.cuh"
 
 namespace sv {
 
@@ -1419,9 +1420,10 @@ static cudaError_t launch_merge_warp_t(const Params& p, cudaStream_t s)
         if (e0 != cudaSuccess) return e0;
         attr = true;
     }
-    cudaError_t e = launch_dependent(k_merge_warp<T>, p,
-                                     (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
-                                     WM_WARPS * 32, WM_SMEM, s);
+    cudaError_t e = p.cand ? launch_dependent(k_merge_cand<T>, p, (unsigned)rows, MC_T, 0, s)
+                           : launch_dependent(k_merge_warp<T>, p,
+                                              (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
+                                              WM_WARPS * 32, WM_SMEM, s);
     if (e != cudaSuccess) return e;
     return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
 }

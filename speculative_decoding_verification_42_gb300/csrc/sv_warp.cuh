@@ -298,32 +298,54 @@ __device__ bool warp_fast_topk(const Params& p, const T* row, int r, int x, Warp
     return true;
 }
 
+// the candidate words of a row the merge loads before it knows their count:
+// word lane + 32 g of the row's array for g < CAND_PREFETCH (two candidates
+// per 16-byte word)
+constexpr int CAND_PREFETCH = 8;
+
 // the top-k of row r from the candidates the stream kernel collected (a flat
-// array and the row's control words, reset here for the next launch): 1 when
-// st is final, 0 when the chunk-key path has to run instead (candidates were
-// lost, or more pass the row threshold than the warp stages)
+// array and the row's control words c4, reset here for the next launch;
+// pre: the prefetched words): 1 when st is final, 0 when the chunk-key path
+// has to run instead (candidates were lost, or more pass the row threshold
+// than the warp stages)
 template <typename T>
-__device__ int warp_cand_topk(const Params& p, int r, int x, WarpSmem& ws, RowStat& st)
+__device__ int warp_cand_topk(const Params& p, int r, int x, WarpSmem& ws, RowStat& st, uint4 c4,
+                              const uint4 (&pre)[CAND_PREFETCH])
 {
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    unsigned* ctl = p.rowctl + (int64_t)r * 4;
-    const uint4 c4 = __ldcg(reinterpret_cast<const uint4*>(ctl));
-    __syncwarp();
-    if (lane == 0) *reinterpret_cast<uint4*>(ctl) = make_uint4(0, 0, 0, 0);
+    if (lane == 0) *reinterpret_cast<uint4*>(p.rowctl + (int64_t)r * 4) = make_uint4(0, 0, 0, 0);
     const uint32_t cnt = c4.x, tau = c4.y, maxkey = c4.z;
     if (maxkey >= 0xFF80u || maxkey <= 0x007Fu) {  // NaN or +inf, or no finite logit
         st.flags = FLAG_NONFINITE;
         return 1;
     }
     if (cnt > (uint32_t)RCAP_ROW || cnt == 0u) return 0;
-    // the candidates, two per 16-byte load, eight loads in flight per lane;
-    // those at or above the row threshold are appended with ballots
     const uint4* src = reinterpret_cast<const uint4*>(p.cand_rows + (int64_t)r * RCAP_ROW);
     const int nw = (int)((cnt + 1u) / 2u);
     int n = 0;
+    // the candidates at or above the row threshold are appended with ballots
+    auto append = [&](const uint4& w, int wi) -> bool {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t key = h ? w.w : w.y;
+            const uint32_t id = h ? w.z : w.x;  // ~0: an unused slot
+            const bool take = wi < nw && 2 * wi + h < (int)cnt && id < (uint32_t)p.V && (key >> 16) >= tau;
+            const unsigned bal = __ballot_sync(FULL, take);
+            if (n + __popc(bal) > WM_CAND) return false;
+            if (take) ws.cand[n + __popc(bal & ((1u << lane) - 1u))] = ((unsigned long long)(~key) << 32) | id;
+            n += __popc(bal);
+        }
+        return true;
+    };
+#pragma unroll
+    for (int g = 0; g < CAND_PREFETCH; ++g) {
+        if (g * 32 >= nw) break;  // warp-uniform
+        if (!append(pre[g], g * 32 + lane)) return 0;
+    }
+    // the rest (more than the prefetch), eight loads in flight per lane
 #pragma unroll 1
-    for (int w0 = 0; w0 < nw; w0 += 32 * 8) {
+    for (int w0 = CAND_PREFETCH * 32; w0 < nw; w0 += 32 * 8) {
         uint4 w[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
@@ -332,21 +354,8 @@ __device__ int warp_cand_topk(const Params& p, int r, int x, WarpSmem& ws, RowSt
         }
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-            const int wi = w0 + g * 32 + lane;
             if (w0 + g * 32 >= nw) break;  // warp-uniform
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t key = h ? w[g].w : w[g].y;
-                const uint32_t id = h ? w[g].z : w[g].x;  // ~0: an unused slot
-                const bool take = wi < nw && 2 * wi + h < (int)cnt && id < (uint32_t)p.V &&
-                                  (key >> 16) >= tau;
-                const unsigned bal = __ballot_sync(FULL, take);
-                if (n + __popc(bal) > WM_CAND) return 0;
-                if (take)
-                    ws.cand[n + __popc(bal & ((1u << lane) - 1u))] =
-                        ((unsigned long long)(~key) << 32) | id;
-                n += __popc(bal);
-            }
+            if (!append(w[g], w0 + g * 32 + lane)) return 0;
         }
     }
     __syncwarp();
@@ -418,8 +427,8 @@ __device__ int warp_sample_list(const Params& p, int tr, const RowStat& ts, bool
         }
         __syncwarp();
     }
-    const float invSt = (float)(1.0 / ts.S);
-    const float invSd = (residual && d.kind == 0) ? (float)(1.0 / d.st.S) : 0.f;
+    const float invSt = 1.f / (float)ts.S;
+    const float invSd = (residual && d.kind == 0) ? 1.f / (float)d.st.S : 0.f;
     const int ept = (n + 31) / 32;
     const int i0 = lane * ept;
     *zero = false;
@@ -464,6 +473,150 @@ __device__ int warp_sample_list(const Params& p, int tr, const RowStat& ts, bool
         return __reduce_max_sync(FULL, tok);
     }
     return -1;
+}
+
+// a row record held in registers (three 16-byte words), as loaded by one lane
+struct RecWords {
+    uint4 a, b, c;
+};
+__device__ __forceinline__ RecWords load_rec(const RowStat* src)
+{
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+    return RecWords{__ldcg(s), __ldcg(s + 1), __ldcg(s + 2)};
+}
+__device__ __forceinline__ RecWords shfl_rec(const RecWords& w, int from)
+{
+    const unsigned FULL = 0xffffffffu;
+    RecWords o;
+    o.a = make_uint4(__shfl_sync(FULL, w.a.x, from), __shfl_sync(FULL, w.a.y, from),
+                     __shfl_sync(FULL, w.a.z, from), __shfl_sync(FULL, w.a.w, from));
+    o.b = make_uint4(__shfl_sync(FULL, w.b.x, from), __shfl_sync(FULL, w.b.y, from),
+                     __shfl_sync(FULL, w.b.z, from), __shfl_sync(FULL, w.b.w, from));
+    o.c = make_uint4(__shfl_sync(FULL, w.c.x, from), __shfl_sync(FULL, w.c.y, from),
+                     __shfl_sync(FULL, w.c.z, from), __shfl_sync(FULL, w.c.w, from));
+    return o;
+}
+__device__ __forceinline__ RowStat rec_stat(const RecWords& w)
+{
+    RowStat r;
+    uint4* d = reinterpret_cast<uint4*>(&r);
+    d[0] = w.a;
+    d[1] = w.b;
+    d[2] = w.c;
+    return r;
+}
+
+// the decision of sequence b by one warp when its rows fit one per lane
+// (2 K_b + 1 <= 32): lane i holds row record i (target rows 0..K_b, then
+// draft rows 0..K_b-1) and slot i's drafted token, all loaded in one round;
+// the same arithmetic and outputs as warp_decide
+template <typename T>
+__device__ bool warp_decide_lanes(const Params& p, int b, int kb, WarpSmem& ws)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int K = p.Kmax, V = p.V;
+    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
+    const int64_t drow0 = (int64_t)b * K * V;
+    RecWords rw{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (lane < nrows)
+        rw = load_rec(p.rstat + (lane <= kb ? target_slot(p, b, lane) : draft_slot(p, b, lane - kb - 1)));
+    const int x = lane < kb ? p.xin[(int64_t)b * K + lane] : -1;
+    const RowStat me = rec_stat(rw);
+    const bool mine = lane < nrows;
+    if (__any_sync(FULL, mine && ((me.flags & FLAG_BLOCK_MERGE) ||
+                                  (me.mode == MODE_LIST && me.n_kept > WM_CAND))))
+        return false;
+    bool nonf = __any_sync(FULL, mine && (me.flags & FLAG_NONFINITE));
+    const bool bad = __any_sync(FULL, lane < kb && (x < 0 || x >= V));
+    float q = 1.f;
+    if (!bad && p.draft_kind == 1) {
+        if (lane < kb) q = __ldcg((const float*)p.draft + drow0 + (int64_t)lane * V + x);
+        nonf |= __any_sync(FULL, lane < kb && (!(q >= 0.f) || q == INFINITY));
+    }
+    if (bad || nonf) {
+        for (int j = lane; j <= K; j += 32) {
+            p.tokens[(int64_t)b * (K + 1) + j] = -1;
+            if (p.lse) p.lse[(int64_t)b * (K + 1) + j] = NAN;
+            if (j < K) {
+                if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
+                if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = NAN;
+            }
+        }
+        if (lane == 0) {
+            p.num_accepted[b] = -1;
+            if (p.row_status) p.row_status[b] = bad ? ROW_BAD_TOKEN : ROW_NONFINITE;
+            if (p.resid_mass) p.resid_mass[b] = NAN;
+            p.jobs[b].kind = JOB_NONE;
+        }
+        return true;
+    }
+    // accept tests, one slot per lane; the first rejection is the lowest
+    // rejecting lane
+    const float pd_row = __shfl_sync(FULL, me.px, min(kb + 1 + lane, 31));
+    const uint4 wrd = lane <= kb ? slot_words(p, b, lane, 0u) : make_uint4(0, 0, 0, 0);
+    bool rej = false;
+    if (lane < kb) {
+        const float pt = me.px;
+        const float pd = p.draft_kind == 1 ? q : pd_row;
+        // IEEE: pd = 0 gives inf or NaN; rounding the ratio to fp32 moves it
+        // by < 1e-7 relative, inside the near-tie window
+        const float ratio = __fdiv_rn(pt, pd);
+        rej = !(u24(wrd.x) < ratio);
+        if (p.p_t_at) p.p_t_at[(int64_t)b * K + lane] = pt;
+        if (p.p_d_at) p.p_d_at[(int64_t)b * K + lane] = pd;
+    }
+    const unsigned rm = __ballot_sync(FULL, rej);
+    const int jstar = rm ? __ffs(rm) - 1 : kb;
+    for (int j = lane; j <= K; j += 32) {
+        if (p.lse) {
+            // lane j holds target row j for j <= kb (kb < 32 here)
+            p.lse[(int64_t)b * (K + 1) + j] = j <= kb ? me.M / p.T + logf((float)me.S) : NAN;
+        }
+        if (j >= kb && j < K) {
+            if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
+            if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = NAN;
+        }
+        if (j != jstar) p.tokens[(int64_t)b * (K + 1) + j] = j < jstar ? x : -1;
+    }
+    const bool residual = jstar < kb;
+    const float u = u24(__shfl_sync(FULL, wrd.y, jstar));
+    const int tr = target_slot(p, b, jstar);
+    const RowStat ts = rec_stat(shfl_rec(rw, jstar));
+    DraftRef d;
+    d.kind = p.draft_kind;
+    d.r = residual ? draft_slot(p, b, jstar) : -1;
+    const RecWords dw = shfl_rec(rw, min(kb + 1 + jstar, 31));
+    if (residual && d.kind == 0) d.st = rec_stat(dw);
+    d.row = residual ? (const void*)((const char*)p.draft +
+                                     (drow0 + (int64_t)jstar * V) * (d.kind == 1 ? 4 : (int64_t)sizeof(T)))
+                     : nullptr;
+    if (ts.mode == MODE_LIST) {
+        unsigned long long Z;
+        bool zero;
+        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, ws, &Z, &zero);
+        if (lane == 0) {
+            p.tokens[(int64_t)b * (K + 1) + jstar] = tok;
+            p.num_accepted[b] = jstar;
+            if (p.row_status) p.row_status[b] = zero ? ROW_ZERO_RESIDUAL : ROW_OK;
+            if (p.resid_mass) p.resid_mass[b] = residual ? (float)from_fix56(Z) : 0.f;
+            p.jobs[b].kind = JOB_NONE;
+        }
+    } else if (lane == 0) {
+        p.tokens[(int64_t)b * (K + 1) + jstar] = -1;
+        p.num_accepted[b] = jstar;
+        if (p.row_status) p.row_status[b] = ROW_OK;
+        if (p.resid_mass && !residual) p.resid_mass[b] = 0.f;
+        Job jb;
+        jb.kind = residual ? JOB_RESIDUAL : JOB_ROW;
+        jb.trow = tr;
+        jb.drow = residual ? d.r : -1;
+        jb.out_idx = b * (K + 1) + jstar;
+        jb.b = b;
+        jb.u = u;
+        p.jobs[b] = jb;
+    }
+    return true;
 }
 
 // true when the warp decided sequence b; false leaves it to the decision grid
@@ -605,6 +758,20 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * WM_WARPS + warp;
     if (r >= p.B * p.rps) return;
+    // every load that does not depend on another goes out at once: the
+    // sequence's K_b, the row's drafted token, its control words and the
+    // first candidate words
+    const int b = r / p.rps, slot = r - b * p.rps;
+    const int jd = slot > p.Kmax ? slot - (p.Kmax + 1) : slot;  // position of the row
+    const int x_raw = jd < p.Kmax ? __ldg(p.xin + (int64_t)b * p.Kmax + jd) : -1;
+    uint4 c4 = make_uint4(0, 0, 0, 0);
+    uint4 pre[CAND_PREFETCH];
+    if (p.cand) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.cand_rows + (int64_t)r * RCAP_ROW);
+        c4 = __ldcg(reinterpret_cast<const uint4*>(p.rowctl + (int64_t)r * 4));
+#pragma unroll
+        for (int g = 0; g < CAND_PREFETCH; ++g) pre[g] = __ldcg(src + g * 32 + lane);
+    }
     const RowRef rr = row_ref(p, r);
     if (!rr.valid) {
         if (lane == 0) report_skipped_row(p, rr);
@@ -615,10 +782,7 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     // the drafted token this row's P(x) is needed at (the bonus row has none)
     int x = -1;
-    if (rr.j < rr.kb) {
-        x = p.xin[(int64_t)rr.b * p.Kmax + rr.j];
-        if (x < 0 || x >= p.V) x = -1;
-    }
+    if (rr.j < rr.kb && x_raw >= 0 && x_raw < p.V) x = x_raw;
     RowStat st;
     st.M = -INFINITY;
     st.kappa = 0;
@@ -630,26 +794,29 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     st.px = 0.f;
     st.pad[0] = st.pad[1] = st.pad[2] = 0;
     if (p.seg_mode == SEG_CHUNK) {
-        const int done = p.cand ? warp_cand_topk<T>(p, r, x, ws, st) : 0;
+        const int done = p.cand ? warp_cand_topk<T>(p, r, x, ws, st, c4, pre) : 0;
         if (!done && !warp_fast_topk<T>(p, row, r, x, ws, st)) st.flags |= FLAG_BLOCK_MERGE;
     } else {
         warp_all_stats(p, r, st);
         if (!st.flags && x >= 0) st.px = row_prob(p, Elem<T>::load_cg(row, x), st.M, st.S);
     }
     if (lane == 0) p.rstat[r] = st;
-    // sequence ticket: every lane's writes are fenced before lane 0 takes it
-    __threadfence();
+    // sequence ticket: the warp barrier orders every lane's writes before lane
+    // 0's fence, which makes them visible before the ticket is taken
     __syncwarp();
     unsigned last = 0;
     if (lane == 0) {
+        __threadfence();
         const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
         last = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
         if (last) p.seq_ticket[rr.b] = 0u;
     }
     last = __shfl_sync(FULL, last, 0);
     if (!last) return;
-    __threadfence();
-    if (warp_decide<T>(p, rr.b, ws)) {
+    if (lane == 0) __threadfence();
+    __syncwarp();
+    const int nrows_b = p.draft_kind == 0 ? 2 * rr.kb + 1 : rr.kb + 1;
+    if (nrows_b <= 32 ? warp_decide_lanes<T>(p, rr.b, rr.kb, ws) : warp_decide<T>(p, rr.b, ws)) {
         __syncwarp();
         if (lane == 0) p.seq_done[rr.b] = 1u;
     }

@@ -100,6 +100,15 @@ def test_candidate_stream(orc, V, dtype, B, K, knobs):
     _check(orc, w)
 
 
+def test_long_drafts(orc):
+    """K_b up to 20: sequences with 2 K_b + 1 > 32 rows are decided by the
+    general (looping) warp decision, shorter ones one row per lane."""
+    w = make_workload("long K", B=10, K_max=20, V=8192, dtype="bf16", target_std=2.5,
+                      draft_noise_std=0.8, ragged_k=(0, 20), seed=123, top_k=40, temperature=0.9)
+    assert (w.k_per_row >= 16).any() and (w.k_per_row < 16).any()
+    _check(orc, w)
+
+
 def test_candidate_stream_heavy_ties(orc):
     """Logits rounded to integers: many logits tie at the bound, so some
     segments overflow their candidate block and those rows take the chunk
