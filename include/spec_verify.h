@@ -179,6 +179,21 @@ spec_status spec_verify_run_noalloc(const spec_verify_config* cfg, const spec_ve
                                     const spec_sampling* s, const spec_verify_outputs* out,
                                     void* stream);
 
+/* Measurement hook (the pages have no counterpart): every later run of the
+ * handle records ev_stage1_begin just before and ev_stage1_end just after its
+ * stage-1 stream kernel (the one that reads the logits) on the run's stream,
+ * so the caller can time that kernel with cudaEventElapsedTime; and when
+ * launches_out is not NULL, each run stores there (host memory, written
+ * before the call returns) the number of kernels it launched.  The events are
+ * cudaEvent_t created by the caller on the handle's device and stay owned by
+ * the caller, who must keep them valid while the hook is set.  Pass NULL for
+ * all three to switch it off.  Returns SPEC_ERR_INVALID_ARG for a NULL handle
+ * or when exactly one of the two events is NULL.  Recording the events may
+ * stop the next kernel from being scheduled before the stream kernel ends, so
+ * a run with the hook set can take slightly longer. */
+spec_status spec_verify_set_profiling(spec_verify_t h, void* ev_stage1_begin, void* ev_stage1_end,
+                                      int32_t* launches_out);
+
 /* Free the handle and its workspace (synchronises its device first). */
 spec_status spec_verify_destroy(spec_verify_t h);
 

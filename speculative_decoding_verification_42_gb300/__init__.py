@@ -27,7 +27,8 @@ SPEC_ROW_OK, SPEC_ROW_BAD_TOKEN, SPEC_ROW_BAD_K, SPEC_ROW_NONFINITE, \
 
 # every function the header declares (checked by the tests)
 ABI_FUNCTIONS = ("spec_verify_create", "spec_verify_run", "spec_draft_sample",
-                 "spec_verify_destroy", "spec_verify_status_string", "spec_verify_run_noalloc")
+                 "spec_verify_destroy", "spec_verify_status_string", "spec_verify_run_noalloc",
+                 "spec_verify_set_profiling")
 SPEC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -93,6 +94,9 @@ def load_library(path: str | None = None) -> C.CDLL:
                                           C.POINTER(spec_sampling), C.POINTER(spec_verify_outputs),
                                           C.c_void_p]
     L.spec_verify_run_noalloc.restype = C.c_int
+    L.spec_verify_set_profiling.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p,
+                                            C.POINTER(C.c_int32)]
+    L.spec_verify_set_profiling.restype = C.c_int
     if path is None:
         _lib = L
     return L
@@ -141,6 +145,16 @@ def spec_verify_run_noalloc(cfg: spec_verify_config, inputs: spec_verify_inputs,
     _check(load_library().spec_verify_run_noalloc(C.byref(cfg), C.byref(inputs), C.byref(sampling),
                                                   C.byref(outputs), C.c_void_p(stream)),
            "spec_verify_run_noalloc")
+
+
+def spec_verify_set_profiling(h, ev_begin: int | None, ev_end: int | None,
+                              launches_out=None) -> None:
+    """Events (cudaEvent_t handles as ints) around the stage-1 stream kernel of
+    later runs, and a ctypes int32 that receives each run's kernel count."""
+    ptr = C.byref(launches_out) if launches_out is not None else None
+    _check(load_library().spec_verify_set_profiling(h, C.c_void_p(ev_begin or 0),
+                                                    C.c_void_p(ev_end or 0), ptr),
+           "spec_verify_set_profiling")
 
 
 def spec_verify_destroy(h) -> None:

@@ -38,6 +38,11 @@ struct spec_verify {
     unsigned long long* cand_rows;  // NULL: this workspace has no candidate arrays
     unsigned* rowctl;
     unsigned* seq_done;
+    // spec_verify_set_profiling: events around the stage-1 stream kernel and
+    // where each run stores the number of kernels it launched (all optional)
+    cudaEvent_t prof_begin;
+    cudaEvent_t prof_end;
+    int32_t* prof_launches;
 };
 
 namespace {
@@ -173,12 +178,16 @@ size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
 // (one warp per row when the knobs allow, else one CTA per row) and decide the
 // sequences, each grid a programmatic dependent launch of the one before
 cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool vec,
-                          cudaStream_t s)
+                          cudaStream_t s, int* launches)
 {
+    if (h->prof_begin && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
     cudaError_t e = p.cand ? launch_stream_cand(p, dtype, h->num_sms, s)
                   : vec    ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
                            : launch_rows(p, dtype, false, s);
     if (e != cudaSuccess) return e;
+    if (h->prof_end && cudaEventRecord(h->prof_end, s) != cudaSuccess) return cudaErrorUnknown;
+    // the merge grid, then (warp merges) the decision grid
+    *launches += warp_merge_ok(p) ? 3 : 2;
     return warp_merge_ok(p) ? launch_merge_warp(p, dtype, s) : launch_merge(p, dtype, s);
 }
 
@@ -315,8 +324,13 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
-    if (launch_stage1(h, p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (!all_lists(p) && launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    int launches = 0;
+    if (launch_stage1(h, p, dtype, vec, cs, &launches) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (!all_lists(p)) {
+        if (launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        ++launches;
+    }
+    if (h->prof_launches) *h->prof_launches = launches;
     return SPEC_OK;
 }
 
@@ -354,10 +368,21 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
-    if (launch_stage1(h, p, dtype, vec, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    int launches = 0;
+    if (launch_stage1(h, p, dtype, vec, cs, &launches) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!all_lists(p) && launch_sample(p, dtype, p.B * p.Kmax, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     if (draft_probs && launch_probs(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+spec_status spec_verify_set_profiling(spec_verify_t h, void* ev_stage1_begin, void* ev_stage1_end,
+                                      int32_t* launches_out)
+{
+    if (!h || (!ev_stage1_begin) != (!ev_stage1_end)) return SPEC_ERR_INVALID_ARG;
+    h->prof_begin = (cudaEvent_t)ev_stage1_begin;
+    h->prof_end = (cudaEvent_t)ev_stage1_end;
+    h->prof_launches = launches_out;
     return SPEC_OK;
 }
 
@@ -417,7 +442,7 @@ size_t layout_over(spec_verify* h, const spec_verify_config* cfg, int32_t batch,
 // bytes of workspace a run of these sizes needs (0: invalid arguments)
 size_t sv_noalloc_bytes(const spec_verify_config* cfg, int32_t batch, int32_t k_max)
 {
-    spec_verify h;
+    spec_verify h{};  // value-initialised: no profiling hook, no pointers
     return layout_over(&h, cfg, batch, k_max, nullptr, 0);
 }
 
@@ -428,7 +453,7 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
                            const spec_verify_outputs* out, void* stream)
 {
     if (!ws || !in) return SPEC_ERR_INVALID_ARG;
-    spec_verify h;
+    spec_verify h{};  // value-initialised: no profiling hook, no pointers
     const size_t need = layout_over(&h, cfg, in->batch, in->k_max, ws, ws_bytes);
     if (need == 0 || need > ws_bytes) return SPEC_ERR_INVALID_ARG;
     h.num_sms = num_sms;
