@@ -82,6 +82,13 @@ enum {
                                 /* only): the token was drawn from p_t; output is valid   */
 };
 
+/* SPEC_TARGET_HIDDEN_LMHEAD (the fused round): `target` is the bf16 hidden
+ * states [B * (k_max + 1), H] of the verified positions and `w_vocab` the bf16
+ * LM head [H, V]; the run first computes the fp32 logits H x W_vocab (fp32
+ * accumulation, tensor cores) into the handle's workspace and verifies them.
+ * It needs target_dtype = SPEC_BF16, hidden = H, draft probabilities
+ * (SPEC_DRAFT_PROBS, SPEC_F32) and H and V multiples of 8 (else create returns
+ * SPEC_ERR_UNSUPPORTED); hidden and w_vocab must start on 16 bytes. */
 typedef struct {
     int32_t device;       /* CUDA device ordinal                                     */
     int32_t max_batch;    /* largest B of any run                                    */
@@ -127,11 +134,12 @@ typedef struct {
                             /* beyond K_b; or NULL                                     */
 } spec_verify_outputs;
 
-/* Allocate a handle and its device workspace on cfg->device.
+/* Allocate a handle and its device workspace on cfg->device (with the LM
+ * head, also the fp32 logits [max_batch * (max_k + 1), V]).
  * Returns SPEC_ERR_INVALID_ARG for sizes < 1 (max_k may be 0) or a dtype/kind
- * combination outside the table above, SPEC_ERR_UNSUPPORTED for the LM-head
- * target kind when this build lacks it, SPEC_ERR_OOM when the workspace does
- * not fit.  On error *out is NULL. */
+ * combination outside the table above, SPEC_ERR_UNSUPPORTED for an LM-head
+ * configuration outside the one described above, SPEC_ERR_OOM when the
+ * workspace does not fit.  On error *out is NULL. */
 spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out);
 
 /* One verify step for a batch (the operation described at the top).  All
@@ -178,6 +186,16 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
 spec_status spec_verify_run_noalloc(const spec_verify_config* cfg, const spec_verify_inputs* in,
                                     const spec_sampling* s, const spec_verify_outputs* out,
                                     void* stream);
+
+/* The LM head alone: logits[m, V] (fp32, row-major, row stride V) =
+ * hidden[m, H] (bf16, row-major) x w_vocab[H, V] (bf16, row-major), fp32
+ * accumulation on the tensor cores, asynchronous on `stream` (the current
+ * device; all pointers device memory owned by the caller, 16-byte aligned).
+ * m = 0 is a no-op.  Returns SPEC_ERR_INVALID_ARG for NULL pointers or sizes
+ * < 1, SPEC_ERR_UNSUPPORTED when H or V is not a multiple of 8 or a pointer is
+ * not on 16 bytes, SPEC_ERR_CUDA when the launch fails. */
+spec_status spec_lmhead_logits(const void* hidden, const void* w_vocab, int32_t m, int32_t hidden_dim,
+                               int32_t vocab, float* logits, void* stream);
 
 /* Measurement hook (the pages have no counterpart): every later run of the
  * handle records ev_stage1_begin just before and ev_stage1_end just after its

@@ -28,7 +28,7 @@ SPEC_ROW_OK, SPEC_ROW_BAD_TOKEN, SPEC_ROW_BAD_K, SPEC_ROW_NONFINITE, \
 # every function the header declares (checked by the tests)
 ABI_FUNCTIONS = ("spec_verify_create", "spec_verify_run", "spec_draft_sample",
                  "spec_verify_destroy", "spec_verify_status_string", "spec_verify_run_noalloc",
-                 "spec_verify_set_profiling")
+                 "spec_verify_set_profiling", "spec_lmhead_logits")
 SPEC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -97,6 +97,9 @@ def load_library(path: str | None = None) -> C.CDLL:
     L.spec_verify_set_profiling.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p,
                                             C.POINTER(C.c_int32)]
     L.spec_verify_set_profiling.restype = C.c_int
+    L.spec_lmhead_logits.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                                     C.c_void_p, C.c_void_p]
+    L.spec_lmhead_logits.restype = C.c_int
     if path is None:
         _lib = L
     return L
@@ -157,6 +160,14 @@ def spec_verify_set_profiling(h, ev_begin: int | None, ev_end: int | None,
            "spec_verify_set_profiling")
 
 
+def spec_lmhead_logits(hidden: int, w_vocab: int, m: int, hidden_dim: int, vocab: int,
+                       logits: int, stream: int = 0) -> None:
+    _check(load_library().spec_lmhead_logits(C.c_void_p(hidden), C.c_void_p(w_vocab), int(m),
+                                             int(hidden_dim), int(vocab), C.c_void_p(logits),
+                                             C.c_void_p(stream)),
+           "spec_lmhead_logits")
+
+
 def spec_verify_destroy(h) -> None:
     _check(load_library().spec_verify_destroy(h), "spec_verify_destroy")
 
@@ -185,14 +196,17 @@ class Verifier:
     """One library handle (its workspace sized for max_batch x max_k x vocab)."""
 
     def __init__(self, *, vocab: int, max_batch: int, max_k: int, dtype, draft_kind: str =
-                 "logits", device: int | None = None):
+                 "logits", device: int | None = None, hidden: int = 0):
+        """hidden > 0: the fused LM head (targets are bf16 hidden states, draft
+        probabilities)."""
         import torch
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.vocab, self.max_batch, self.max_k = vocab, max_batch, max_k
         dt = SPEC_BF16 if dtype in ("bf16", torch.bfloat16) else SPEC_F32
         dk = SPEC_DRAFT_PROBS if draft_kind == "probs" else SPEC_DRAFT_LOGITS
-        self.cfg = spec_verify_config(self.device, max_batch, max_k, vocab, 0,
-                                      SPEC_TARGET_LOGITS, dt, dk,
+        kind = SPEC_TARGET_HIDDEN_LMHEAD if hidden else SPEC_TARGET_LOGITS
+        self.cfg = spec_verify_config(self.device, max_batch, max_k, vocab, int(hidden),
+                                      kind, dt, dk,
                                       SPEC_F32 if dk == SPEC_DRAFT_PROBS else dt)
         self.h = spec_verify_create(self.cfg)
 
@@ -214,11 +228,17 @@ class Verifier:
 
     def run(self, target, draft, draft_tokens, k_per_row=None, *, temperature=1.0, top_k=0,
             top_p=1.0, seed=0, round=0, out: dict | None = None, debug: bool = True,
-            stream=None) -> dict:
-        """Verify a batch; returns (and fills) a dict of output tensors."""
+            stream=None, w_vocab=None) -> dict:
+        """Verify a batch; returns (and fills) a dict of output tensors.  With the
+        LM head, ``target`` is the hidden states [B * (K + 1), H] and ``w_vocab``
+        the [H, V] matrix."""
         import torch
-        B, K1, V = target.shape
-        K = K1 - 1
+        if w_vocab is not None:
+            B, K = draft.shape[0], draft.shape[1]
+            V = draft.shape[2]
+        else:
+            B, K1, V = target.shape
+            K = K1 - 1
         dev = target.device
         if out is None:
             out = dict(tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
@@ -230,7 +250,7 @@ class Verifier:
                            residual_mass=torch.empty(B, dtype=torch.float32, device=dev),
                            target_lse=torch.empty((B, K + 1), dtype=torch.float32,
                                                   device=dev))
-        ins = spec_verify_inputs(_ptr(target), None, _ptr(draft), _ptr(draft_tokens),
+        ins = spec_verify_inputs(_ptr(target), _ptr(w_vocab), _ptr(draft), _ptr(draft_tokens),
                                  _ptr(k_per_row), B, K)
         outs = spec_verify_outputs(*[_ptr(out.get(f)) for f, _ in spec_verify_outputs._fields_])
         s = stream if stream is not None else torch.cuda.current_stream(dev)

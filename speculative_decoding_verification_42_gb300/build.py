@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libspec_verify.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["sv_rows.cu", "sv_sample.cu", "sv_api.cu", "sv_noalloc.cu"]
+SOURCES = ["sv_rows.cu", "sv_sample.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lmhead.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
               "-Xptxas", "-warn-spills"]

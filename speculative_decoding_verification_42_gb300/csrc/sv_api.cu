@@ -43,6 +43,7 @@ struct spec_verify {
     cudaEvent_t prof_begin;
     cudaEvent_t prof_end;
     int32_t* prof_launches;
+    float* logits;        // the LM head's output (SPEC_TARGET_HIDDEN_LMHEAD), else NULL
 };
 
 namespace {
@@ -149,6 +150,9 @@ size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
     const size_t o_err = take(sizeof(unsigned));
     const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
     const size_t o_ctl = take(sizeof(unsigned) * 4 * h->rows_cap);
+    const bool lmhead = cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
+    const size_t o_logits =
+        lmhead ? take(sizeof(float) * (size_t)cfg->max_batch * (cfg->max_k + 1) * (size_t)V) : 0;
     const size_t o_cand = with_cand ? take(sizeof(unsigned long long) * RCAP_ROW * h->rows_cap) : 0;
     if (base) {
         char* b = (char*)base;
@@ -168,6 +172,7 @@ size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
         h->err = (unsigned*)(b + o_err);
         h->seq_done = (unsigned*)(b + o_sd);
         h->rowctl = (unsigned*)(b + o_ctl);
+        h->logits = lmhead ? (float*)(b + o_logits) : nullptr;
         h->cand_rows = with_cand ? (unsigned long long*)(b + o_cand) : nullptr;
     }
     return off;
@@ -237,8 +242,15 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
         return SPEC_ERR_INVALID_ARG;
     }
     if (cfg->max_k > 255) return SPEC_ERR_UNSUPPORTED;  // a decision stages 2*K_max+1 rows
-    if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD) return SPEC_ERR_UNSUPPORTED;
-    if (cfg->target_kind != SPEC_TARGET_LOGITS) return SPEC_ERR_INVALID_ARG;
+    if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD) {
+        // bf16 hidden states and W_vocab, fp32 draft probabilities; the tensor
+        // maps want row strides on 16 bytes
+        if (cfg->hidden < 1 || cfg->target_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+        if (cfg->draft_kind != SPEC_DRAFT_PROBS || cfg->hidden % 8 || cfg->vocab % 8)
+            return SPEC_ERR_UNSUPPORTED;
+    } else if (cfg->target_kind != SPEC_TARGET_LOGITS) {
+        return SPEC_ERR_INVALID_ARG;
+    }
     // the stage-2 sampler scans at most NT segments per row
     if ((int64_t)cfg->vocab > (int64_t)NT * SAMPLE_SEG) return SPEC_ERR_UNSUPPORTED;
     if ((int64_t)cfg->max_batch * (2 * (int64_t)cfg->max_k + 1) > (int64_t)INT32_MAX / 4)
@@ -292,6 +304,10 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     if (in->batch == 0) return SPEC_OK;
     if (!in->target || !in->draft || !out->tokens || !out->num_accepted) return SPEC_ERR_INVALID_ARG;
     if (in->k_max > 0 && !in->draft_tokens) return SPEC_ERR_INVALID_ARG;
+    const bool lmhead = cfg.target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
+    const int m_rows = in->batch * (in->k_max + 1);  // verified positions (LM-head rows)
+    if (lmhead && (!in->w_vocab || !lmhead_shape_ok(in->target, in->w_vocab, m_rows, cfg.vocab, cfg.hidden)))
+        return SPEC_ERR_INVALID_ARG;
 
     p.B = in->batch;
     p.Kmax = in->k_max;
@@ -299,7 +315,8 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     p.rps = 2 * in->k_max + 1;
     p.draft_launch = 0;
     p.draft_kind = cfg.draft_kind;
-    p.target = in->target;
+    // with the LM head the verify reads the fp32 logits it writes to the workspace
+    p.target = lmhead ? (const void*)h->logits : in->target;
     p.draft = in->draft;
     p.xin = in->draft_tokens;
     p.kpr = in->k_per_row;
@@ -312,9 +329,9 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     p.lse = out->target_lse;
     p.probs_out = nullptr;
     fill_workspace(h, p);
-    const int dtype = cfg.target_dtype;
+    const int dtype = lmhead ? SPEC_F32 : cfg.target_dtype;
     choose_seg_mode(p, dtype);
-    const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(in->target) &&
+    const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(p.target) &&
                      (cfg.draft_kind == SPEC_DRAFT_PROBS || aligned16(in->draft));
     // top-k rows: candidates written while each segment is in shared memory
     p.npiece = (int)cdiv((int64_t)p.V * elem_size(dtype), CS_PIECE);
@@ -325,6 +342,12 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
     int launches = 0;
+    if (lmhead) {
+        if (launch_lmhead(in->target, in->w_vocab, h->logits, m_rows, cfg.vocab, cfg.hidden, cfg.vocab,
+                          h->err, cs) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        ++launches;
+    }
     if (launch_stage1(h, p, dtype, vec, cs, &launches) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!all_lists(p)) {
         if (launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -373,6 +396,19 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
     if (!all_lists(p) && launch_sample(p, dtype, p.B * p.Kmax, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     if (draft_probs && launch_probs(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+spec_status spec_lmhead_logits(const void* hidden, const void* w_vocab, int32_t m, int32_t hidden_dim,
+                               int32_t vocab, float* logits, void* stream)
+{
+    if (!hidden || !w_vocab || !logits || m < 0 || hidden_dim < 1 || vocab < 1) return SPEC_ERR_INVALID_ARG;
+    if (m == 0) return SPEC_OK;
+    if (!lmhead_shape_ok(hidden, w_vocab, m, vocab, hidden_dim) || ((uintptr_t)logits & 15u))
+        return SPEC_ERR_UNSUPPORTED;
+    if (launch_lmhead(hidden, w_vocab, logits, m, vocab, hidden_dim, vocab, nullptr, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 

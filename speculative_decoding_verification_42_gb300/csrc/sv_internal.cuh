@@ -548,6 +548,10 @@ __host__ __device__ __forceinline__ bool warp_merge_ok(const Params& p)
                                (p.seg_mode == SEG_SUM && p.top_k == 0 && !(p.top_p < 1.0f)));
 }
 cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s);
+// the LM head: out[M, N] (row stride ldo) = hidden[M, K] x w[K, N], bf16 in, fp32 out
+bool lmhead_shape_ok(const void* hidden, const void* w, int M, int N, int K);
+cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, int N, int K, int64_t ldo,
+                          unsigned* err, cudaStream_t s);
 cudaError_t launch_probs(const Params& p, int dtype, cudaStream_t s);
 
 }  // namespace sv

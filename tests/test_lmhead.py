@@ -1,0 +1,117 @@
+"""The LM head of the fused verify round (logits = H x W_vocab, bf16 inputs,
+fp32 accumulation on the tensor cores), through the C ABI.
+
+Logits are checked element by element against the fp64 oracle GEMM and a plain
+PyTorch fp32 matmul with the fp32-accumulation bound of an H-term dot product,
+|d| <= 1e-5 * sum_k |h_k w_k| + 1e-6; the fused verify is checked for token
+parity against the oracle verifying the same (GPU) logits."""
+import numpy as np
+import pytest
+
+from parity_util import DELTA, compare, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_42_gb300 import build
+    build.build()
+
+
+def _bf16(rng, shape, std):
+    from workloads.synth import f32_to_bf16_bits
+    return f32_to_bf16_bits((rng.standard_normal(shape, dtype=np.float32) * np.float32(std)))
+
+
+def _gpu_logits(h_bits, w_bits):
+    import torch
+    import speculative_decoding_verification_42_gb300 as sv
+    M, H = h_bits.shape
+    V = w_bits.shape[1]
+    h, w = to_device(h_bits), to_device(w_bits)
+    out = torch.full((M, V), float("nan"), dtype=torch.float32, device="cuda")
+    sv.spec_lmhead_logits(h.data_ptr(), w.data_ptr(), M, H, V, out.data_ptr(),
+                          torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return out, h, w
+
+
+def _bound(h_bits, w_bits, rows):
+    from workloads.synth import bf16_bits_to_f32
+    ha = np.abs(bf16_bits_to_f32(h_bits[rows]).astype(np.float64))
+    wa = np.abs(bf16_bits_to_f32(w_bits).astype(np.float64))
+    return 1e-5 * (ha @ wa) + 1e-6
+
+
+@pytest.mark.parametrize("M,H,V", [(256, 512, 2048), (200, 136, 1000), (128, 64, 256),
+                                   (384, 1024, 4104)])
+def test_lmhead_small(orc, M, H, V):
+    """Whole tiles, and ragged M, H (not a multiple of the 64-deep slice) and V."""
+    rng = np.random.default_rng(M + H + V)
+    hb, wb = _bf16(rng, (M, H), 1.0), _bf16(rng, (H, V), 0.02)
+    g, h, w = _gpu_logits(hb, wb)
+    got = g.cpu().numpy().astype(np.float64)
+    want = orc.lmhead(hb, wb)
+    bound = _bound(hb, wb, slice(None))
+    assert np.isfinite(got).all()
+    assert (np.abs(got - want) <= bound).all(), float((np.abs(got - want) / bound).max())
+    # the plain PyTorch fp32 reference of the same product
+    import torch
+    ref = (h.float() @ w.float()).cpu().numpy().astype(np.float64)
+    assert (np.abs(got - ref) <= 2 * bound).all()
+
+
+def test_lmhead_config5_shape(orc):
+    """The fused workload's GEMM (256 x 8192 x 128256): every logit against the
+    PyTorch fp32 product, three rows against the fp64 oracle."""
+    import torch
+    from workloads import make_config
+    w5 = make_config(5)
+    g, h, w = _gpu_logits(w5.hidden, w5.w_vocab)
+    ref = (h.float() @ w.float())
+    rows = [0, 131, 255]
+    got = g.cpu().numpy()
+    for r in rows:
+        o = orc.lmhead(w5.hidden, w5.w_vocab, r, r + 1)[0]
+        b = _bound(w5.hidden, w5.w_vocab, [r])[0]
+        assert (np.abs(got[r].astype(np.float64) - o) <= b).all()
+    diff = (g - ref).abs()
+    # sum_k |h w| ~ 8192 * 0.8 * 0.016 ~ 105; the bound is ~1.1e-3
+    assert float(diff.max()) < 2e-3, float(diff.max())
+
+
+def test_fused_verify_config5_reduced(orc):
+    """The fused round (LM head + verify, draft probabilities) on the config-5
+    recipe at B = 8: tokens, statuses and probabilities against the oracle
+    verifying the GPU's own logits."""
+    import torch
+    import speculative_decoding_verification_42_gb300 as sv
+    from workloads.synth import make_lmhead_workload
+    B, K, V, H = 8, 7, 128256, 8192
+    w5 = make_lmhead_workload("fused B=8", B=B, K_max=K, V=V, H=H, temperature=0.8, seed=4)
+    g, h, w = _gpu_logits(w5.hidden, w5.w_vocab)
+    logits = g.cpu().numpy().reshape(B, K + 1, V)
+    # draft probabilities: softmax((target logits + noise) / T), as the recipe says
+    q = np.empty((B, K, V), np.float32)
+    for b in range(B):
+        for j in range(K):
+            q[b, j] = orc.row_probs((logits[b, j] + w5.draft_noise[b, j]).astype(np.float32),
+                                    w5.temperature)[0].astype(np.float32)
+    w5.target, w5.draft, w5.draft_kind = np.ascontiguousarray(logits), q, "probs"
+    toks, _ = orc.draft_sample(q, w5.k_per_row, draft_kind=orc.DRAFT_PROBS,
+                               temperature=w5.temperature, seed=w5.seed)
+    ver = sv.Verifier(vocab=V, max_batch=B, max_k=K, dtype="bf16", draft_kind="probs", hidden=H)
+    xt = torch.from_numpy(np.ascontiguousarray(toks, dtype=np.int32)).cuda()
+    kpr = torch.from_numpy(w5.k_per_row).cuda()
+    out = ver.run(h, torch.from_numpy(q).cuda(), xt, kpr, temperature=w5.temperature,
+                  seed=w5.seed, w_vocab=w)
+    torch.cuda.synchronize()
+    gout = {k: v.cpu().numpy() for k, v in out.items()}
+    ver.close()
+    o = run_oracle(orc, w5, toks)
+    n_near = compare(gout, o, w5, toks)
+    assert n_near <= 1
