@@ -43,6 +43,14 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def _stage1_kernel(w) -> str:
     """The kernel that streams the logits for this workload's knobs."""
     row_bytes = w.V * (2 if w.dtype == "bf16" else 4)
@@ -75,13 +83,19 @@ def _workload(n: int):
 
 
 def _wl_config(w, n_rot):
-    return {
+    cfg = {
         "workload": w.name, "config_id": None, "B": w.B, "K": w.K_max, "V": w.V,
         "input_dtype": w.dtype, "temperature": w.temperature, "top_k": w.top_k,
         "top_p": w.top_p, "rows_per_step": w.rows(), "logit_bytes_per_step": w.logit_bytes(),
         "l2": f"{n_rot} rotating input copies ({n_rot * w.logit_bytes() / 1e6:.0f} MB) > L2",
         "parallelism": "replicas (one batch per GPU)",
     }
+    if w.hidden is not None:
+        wb = w.w_vocab.size * 2
+        cfg.update(H=int(w.hidden.shape[1]), input_dtype="bf16 hidden states, bf16 W_vocab, "
+                   "f32 draft probabilities", logit_bytes_per_step=None,
+                   l2=f"every step reads W_vocab ({wb / 1e9:.2f} GB) > L2")
+    return cfg
 
 
 # --------------------------------------------------------------------------- #
@@ -169,6 +183,35 @@ def cpu_baseline(w, toks, seconds_target: float = 15.0, max_seq: int | None = No
             "host": _host()}
 
 
+def _fused_seq(oracle, w, probs, toks, b):
+    """One sequence of the fused round on the host: the fp64 LM head of its
+    K+1 hidden rows, then the verify against its draft probabilities."""
+    K1 = w.K_max + 1
+    lg = oracle.lmhead(w.hidden, w.w_vocab, b * K1, (b + 1) * K1).astype(np.float32)
+    return oracle.verify(lg.reshape(1, K1, w.V), probs[b:b + 1], toks[b:b + 1],
+                         w.k_per_row[b:b + 1], draft_kind=oracle.DRAFT_PROBS,
+                         temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                         seed=w.seed, round=w.round)
+
+
+def cpu_baseline_fused(w, probs, toks, seconds_target: float = 15.0):
+    import oracle
+    t0 = time.perf_counter()
+    rows = nseq = 0
+    while True:
+        b = nseq % w.B
+        _fused_seq(oracle, w, probs, toks, b)
+        rows += int(w.k_per_row[b]) + 1
+        nseq += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target:
+            break
+    return {"value": rows / el, "unit": UNIT, "cores": oracle.cores_used(), "kind": "oracle",
+            "sample": f"{nseq} sequences ({rows} rows) of the same workload: fp64 LM head "
+                      f"of the sequence's hidden rows + the verify, {el:.1f} s single-threaded",
+            "host": _host()}
+
+
 def _host():
     try:
         model = ""
@@ -191,44 +234,78 @@ def run_reference(args):
         return
     import oracle
     w = _workload(args.config)
-    dk = oracle.DRAFT_PROBS if w.draft_kind == "probs" else oracle.DRAFT_LOGITS
-    toks, _ = oracle.draft_sample(w.draft, w.k_per_row, draft_kind=dk,
-                                  temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
-                                  seed=w.seed, round=w.round)
+    fused = w.hidden is not None
     per_step = max(1, args.ref_seq)
-    for i in range(args.warmup):
-        b = i % w.B
-        oracle.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
-                      temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed,
-                      b_begin=b, b_end=b + 1)
-        if i >= 2:
-            break
-    t0 = time.perf_counter()
+    if fused:
+        # per sequence, untimed: the draft probabilities softmax((target
+        # logits + noise) / T) and the drafted tokens; timed: the LM head of
+        # the sequence's rows and its verify
+        cache = {}
+
+        def prep(b):
+            if b not in cache:
+                K1 = w.K_max + 1
+                lg = oracle.lmhead(w.hidden, w.w_vocab, b * K1, b * K1 + w.K_max)
+                q = np.stack([oracle.row_probs((lg[j] + w.draft_noise[b, j]).astype(np.float32),
+                                               w.temperature)[0] for j in range(w.K_max)])
+                q = q.astype(np.float32)[None]
+                t, _ = oracle.draft_sample(q, w.k_per_row[b:b + 1], draft_kind=oracle.DRAFT_PROBS,
+                                           temperature=w.temperature, seed=w.seed, round=w.round)
+                cache.clear()
+                cache[b] = (q, t)
+            return cache[b]
+
+        def one(b):
+            q, t = prep(b)
+            t0 = time.perf_counter()
+            _fused_seq(oracle, w, q, t, 0)
+            return time.perf_counter() - t0
+    else:
+        dk = oracle.DRAFT_PROBS if w.draft_kind == "probs" else oracle.DRAFT_LOGITS
+        toks, _ = oracle.draft_sample(w.draft, w.k_per_row, draft_kind=dk,
+                                      temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                                      seed=w.seed, round=w.round)
+
+        def one(b):
+            t0 = time.perf_counter()
+            oracle.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
+                          temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
+                          seed=w.seed, round=w.round, b_begin=b, b_end=b + 1)
+            return time.perf_counter() - t0
+
+    for i in range(min(args.warmup, 1 if fused else 3)):
+        one(i % w.B)
+    el = 0.0
     rows = 0
+    steps = 0
     for s in range(args.steps):
         for q in range(per_step):
             b = (s * per_step + q) % w.B
-            oracle.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
-                          temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
-                          seed=w.seed, b_begin=b, b_end=b + 1)
+            el += one(b)
             rows += int(w.k_per_row[b]) + 1
-    el = time.perf_counter() - t0
+        steps += 1
+        if el >= args.ref_seconds:
+            break  # a bounded sample: the oracle is slow by design
     value = rows / el
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _wl_config(w, 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.cores_used(),
                          "kind": "oracle",
-                         "sample": f"{per_step} sequence(s) per step of the same workload",
+                         "sample": f"{steps} step(s) of {per_step} sequence(s) of the same "
+                                   f"workload ({rows} rows, {el:.1f} s timed)"
+                                   + ("; each: fp64 LM head + verify" if fused else ""),
                          "host": _host()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     line["config"]["l2"] = "n/a: host memory"
+    line["config"]["config_id"] = args.config
     line["config"]["note"] = ("reference arm: the fp64 CPU oracle (this project's checker) on "
-                              "the host cores; the pages ship no implementation")
+                              "the host cores; the pages ship no implementation; the timed "
+                              f"loop stops after {args.ref_seconds:.0f} s of oracle time")
     print(json.dumps(line), flush=True)
 
 
@@ -257,24 +334,49 @@ def run_gpu(args):
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(a).to(dev)
 
-    target = [to_dev(w.target)]
-    draft = [to_dev(w.draft)]
-    for _ in range(ROTATE - 1):
-        target.append(target[0].clone())
-        draft.append(draft[0].clone())
+    stream = torch.cuda.current_stream(dev)
     kpr = torch.from_numpy(w.k_per_row).to(dev)
-    ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype=w.dtype, device=local,
-                      draft_kind=w.draft_kind)
     knobs = dict(temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed)
-    # drafted tokens: the library's draft-side sampler (tag-1 uniforms)
-    toks = ver.draft_sample(draft[0], kpr, **knobs)
+    fused = w.hidden is not None
+    if fused:
+        # the fused round: hidden states x W_vocab, then the verify against
+        # draft probabilities softmax((target logits + noise) / T) (the
+        # workload's recipe, prepared once here); W (2.1 GB) exceeds L2
+        H = w.hidden.shape[1]
+        hid = to_dev(w.hidden)
+        wv = to_dev(w.w_vocab)
+        logits = torch.empty((w.B * (w.K_max + 1), w.V), dtype=torch.float32, device=dev)
+        sv.spec_lmhead_logits(hid.data_ptr(), wv.data_ptr(), logits.shape[0], H, w.V,
+                              logits.data_ptr(), stream.cuda_stream)
+        lg = logits.view(w.B, w.K_max + 1, w.V)[:, :w.K_max]
+        probs = torch.softmax((lg + to_dev(w.draft_noise)) / w.temperature, dim=-1).contiguous()
+        del logits, lg
+        ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype="bf16", device=local,
+                          draft_kind="probs", hidden=H)
+        # drafted tokens x ~ P_d: inputs of the round, drawn once by torch
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed)
+        toks = torch.multinomial(probs.view(-1, w.V), 1, generator=gen)
+        toks = toks.view(w.B, w.K_max).to(torch.int32).contiguous()
+        target = [hid] * ROTATE
+        draft = [probs] * ROTATE
+    else:
+        target = [to_dev(w.target)]
+        draft = [to_dev(w.draft)]
+        for _ in range(ROTATE - 1):
+            target.append(target[0].clone())
+            draft.append(draft[0].clone())
+        ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype=w.dtype, device=local,
+                          draft_kind=w.draft_kind)
+        # drafted tokens: the library's draft-side sampler (tag-1 uniforms)
+        toks = ver.draft_sample(draft[0], kpr, **knobs)
     torch.cuda.synchronize()
     out = None
-    stream = torch.cuda.current_stream(dev)
 
     def step(i, o):
         c = i % ROTATE
-        return ver.run(target[c], draft[c], toks, kpr, out=o, debug=False, **knobs)
+        return ver.run(target[c], draft[c], toks, kpr, out=o, debug=False,
+                       w_vocab=wv if fused else None, **knobs)
 
     out = step(0, None)
     for i in range(max(3, args.warmup)):
@@ -332,10 +434,18 @@ def run_gpu(args):
 
     rows = w.rows()
     value = rows * K * world / (total_ms / 1e3)
-    bytes_step = w.logit_bytes()
     peak, peak_src = _peaks()
+    if fused:
+        # the LM head: reads H and W, writes the fp32 logits
+        M = w.B * (w.K_max + 1)
+        bytes_step = (w.hidden.size + w.w_vocab.size) * 2 + M * w.V * 4
+        flops = 2.0 * M * H * w.V
+        kernel = "k_lmhead"
+    else:
+        bytes_step = w.logit_bytes()
+        flops = None
+        kernel = _stage1_kernel(w)
     achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
-    kernel = _stage1_kernel(w)
 
     # end to end: host buffers through the same call, copies inside the timed region
     e2e = None
@@ -357,7 +467,8 @@ def run_gpu(args):
             draft[c].copy_(h_draft, non_blocking=True)
             d_toks.copy_(h_toks, non_blocking=True)
             d_kpr.copy_(h_kpr, non_blocking=True)
-            o = ver.run(target[c], draft[c], d_toks, d_kpr, out=out, debug=False, **knobs)
+            o = ver.run(target[c], draft[c], d_toks, d_kpr, out=out, debug=False,
+                        w_vocab=wv if fused else None, **knobs)
             h_out_t.copy_(o["tokens"], non_blocking=True)
             h_out_n.copy_(o["num_accepted"], non_blocking=True)
 
@@ -391,7 +502,11 @@ def run_gpu(args):
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(w, toks.cpu().numpy(), seconds_target=args.cpu_seconds)
+        if fused:
+            cpu = cpu_baseline_fused(w, draft[0].cpu().numpy(), toks.cpu().numpy(),
+                                     seconds_target=args.cpu_seconds)
+        else:
+            cpu = cpu_baseline(w, toks.cpu().numpy(), seconds_target=args.cpu_seconds)
     cfg = _wl_config(w, ROTATE)
     cfg["config_id"] = args.config
     line = {
@@ -411,6 +526,13 @@ def run_gpu(args):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clocks,
     }
+    if flops:
+        tf = _tensor_peak()
+        line["roofline"]["tensor"] = {
+            "achieved_tflops": flops / (mean_kern_ms / 1e3) / 1e12, "peak_tflops": tf,
+            "frac": flops / (mean_kern_ms / 1e3) / 1e12 / tf if tf else None,
+            "flops_per_launch": flops,
+            "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json), burst"}
     print(json.dumps(line), flush=True)
     ver.close()
     if dist:
@@ -422,13 +544,15 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seq", type=int, default=1,
                     help="reference arm: sequences verified by the oracle per step")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: stop the timed loop after this much oracle time")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         run_reference(args)

@@ -198,8 +198,10 @@ spec_status spec_lmhead_logits(const void* hidden, const void* w_vocab, int32_t 
                                int32_t vocab, float* logits, void* stream);
 
 /* Measurement hook (the pages have no counterpart): every later run of the
- * handle records ev_stage1_begin just before and ev_stage1_end just after its
- * stage-1 stream kernel (the one that reads the logits) on the run's stream,
+ * handle records ev_stage1_begin just before and ev_stage1_end just after the
+ * kernel that reads the run's bulk input (the stage-1 stream kernel over the
+ * logits, or the LM head over W_vocab when the target is hidden states) on the
+ * run's stream,
  * so the caller can time that kernel with cudaEventElapsedTime; and when
  * launches_out is not NULL, each run stores there (host memory, written
  * before the call returns) the number of kernels it launched.  The events are

@@ -183,14 +183,15 @@ size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
 // (one warp per row when the knobs allow, else one CTA per row) and decide the
 // sequences, each grid a programmatic dependent launch of the one before
 cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool vec,
-                          cudaStream_t s, int* launches)
+                          cudaStream_t s, int* launches, bool timed = true)
 {
-    if (h->prof_begin && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
+    const bool rec = timed && h->prof_begin;
+    if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
     cudaError_t e = p.cand ? launch_stream_cand(p, dtype, h->num_sms, s)
                   : vec    ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
                            : launch_rows(p, dtype, false, s);
     if (e != cudaSuccess) return e;
-    if (h->prof_end && cudaEventRecord(h->prof_end, s) != cudaSuccess) return cudaErrorUnknown;
+    if (rec && cudaEventRecord(h->prof_end, s) != cudaSuccess) return cudaErrorUnknown;
     // the merge grid, then (warp merges) the decision grid
     *launches += warp_merge_ok(p) ? 3 : 2;
     return warp_merge_ok(p) ? launch_merge_warp(p, dtype, s) : launch_merge(p, dtype, s);
@@ -343,12 +344,15 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     cudaStream_t cs = (cudaStream_t)stream;
     int launches = 0;
     if (lmhead) {
+        // the hook times the LM head, the kernel that reads W_vocab
+        if (h->prof_begin && cudaEventRecord(h->prof_begin, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         if (launch_lmhead(in->target, in->w_vocab, h->logits, m_rows, cfg.vocab, cfg.hidden, cfg.vocab,
                           h->err, cs) != cudaSuccess)
             return SPEC_ERR_CUDA;
+        if (h->prof_end && cudaEventRecord(h->prof_end, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;
     }
-    if (launch_stage1(h, p, dtype, vec, cs, &launches) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!all_lists(p)) {
         if (launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;
