@@ -7,16 +7,20 @@
 // Sampling", The cost of one token, is the target model's forward pass that
 // produces these logits).
 //
-// One CTA computes a 128 x 256 tile of logits on the 5th-generation tensor
-// cores: lane 0 of warp 0 streams 64-deep K slices of H and W into a
-// four-stage shared-memory ring with tensor-map bulk copies (128-byte
-// swizzle); lane 0 of warp 1 issues tcgen05.mma (kind::f16, bf16 x bf16 ->
-// fp32, M = 128, N = 256, K = 16 per instruction) into a tensor-memory
-// accumulator and releases each stage with tcgen05.commit; after the last
-// slice the four warps read the accumulator back (tcgen05.ld, one row per
-// thread) and store the fp32 tile.  H is the K-major A operand; W, whose rows
-// run along the vocabulary, is the N-major B operand.
+// Persistent clusters of two CTAs on neighbouring 128-row blocks of H share
+// each 64-deep K slice of W: every CTA copies half of the slice's 256 columns
+// and multicasts it to both (W crosses HBM once), and its own 128 rows of H.
+// Per CTA, lane 0 of warp 0 fills a four-stage shared-memory ring with
+// tensor-map bulk copies (128-byte swizzle); lane 0 of warp 1 issues
+// tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 256, K = 16) into
+// one of two tensor-memory accumulators and frees each stage in both CTAs
+// with a multicast tcgen05.commit; warps 2..5 read the other accumulator back
+// (tcgen05.ld, one row per thread) and store the fp32 tile meanwhile.  H is
+// the K-major A operand; W, whose rows run along the vocabulary, is the
+// N-major B operand.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
+
+#include <algorithm>
 
 #include "sv_internal.cuh"
 #include "spec_verify.h"
@@ -29,7 +33,10 @@ constexpr int LM_B_BYTES = LM_BK * LM_BN * 2;      // 32 KB: four 64-column boxe
 constexpr int LM_BOX_B = LM_BK * 64 * 2;           // 8 KB: one W box (64 K-rows x 64 columns)
 constexpr int LM_STAGE_BYTES = LM_A_BYTES + LM_B_BYTES;
 constexpr int LM_SMEM = LM_STAGES * LM_STAGE_BYTES + 1024;  // + slack for 1024-byte alignment
-constexpr uint32_t LM_TMEM_COLS = 256;              // fp32 accumulator: 128 lanes x 256 columns
+constexpr int LM_THREADS = 192;                     // producer, MMA, four epilogue warps
+constexpr uint32_t LM_ACC_COLS = 256;               // fp32 accumulator: 128 lanes x 256 columns
+constexpr uint32_t LM_TMEM_COLS = 2 * LM_ACC_COLS;  // two accumulators
+static_assert(LM_BN == 4 * 64, "each CTA of the pair copies two 64-column boxes of W");
 
 // ------------------------------------------------------------------------- //
 // PTX wrappers                                                              //
@@ -40,6 +47,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// the same box into the same shared-memory offset of every CTA in cta_mask,
+// completing on the mbarrier at the same offset in each
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 
@@ -69,6 +89,31 @@ __device__ __forceinline__ void lm_commit(uint64_t* bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(bar)) : "memory");
 }
+// the same, arriving on the mbarrier at bar's offset in every CTA of cta_mask
+__device__ __forceinline__ void lm_commit_mc(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
+}
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// a bounded wait that also gives up once another role of the CTA has failed
+__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, const volatile int* failed)
+{
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && *failed) return false;
+    }
+    return false;
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -90,24 +135,31 @@ __device__ __forceinline__ void lm_ld32(uint32_t taddr, uint32_t (&v)[32])
 }
 
 // ------------------------------------------------------------------------- //
-// k_lmhead: one 128 x 256 tile of logits per CTA (grid: N tiles x M tiles)  //
+// k_lmhead: persistent two-CTA clusters; cluster c takes the tiles c, c + C, //
+// c + 2C, ... of (pairs of 128-row blocks) x (256-column blocks)            //
 // ------------------------------------------------------------------------- //
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(LM_THREADS, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
              float* __restrict__ out, int M, int N, int K, int64_t ldo, unsigned* err)
 {
     extern __shared__ unsigned char lm_smem_raw[];
-    __shared__ __align__(8) uint64_t full[LM_STAGES];
-    __shared__ __align__(8) uint64_t empty[LM_STAGES];
-    __shared__ __align__(8) uint64_t done;
+    __shared__ __align__(8) uint64_t full[LM_STAGES];   // stage loaded (own H + both W halves)
+    __shared__ __align__(8) uint64_t empty[LM_STAGES];  // stage read by both CTAs' MMAs
+    __shared__ __align__(8) uint64_t acc_full[2];       // accumulator complete
+    __shared__ __align__(8) uint64_t acc_empty[2];      // accumulator read back
     __shared__ uint32_t tmem_slot;
     __shared__ int failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // stage buffers on a 1024-byte boundary (the period of the 128-byte swizzle)
+    const uint32_t rank = cluster_rank();
+    // stage buffers on a 1024-byte boundary (the period of the 128-byte
+    // swizzle); the offset is the same in both CTAs of the cluster
     const uint32_t raw = smem_u32(lm_smem_raw);
     unsigned char* base = lm_smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    const int m0 = blockIdx.y * LM_BM, n0 = blockIdx.x * LM_BN;
     const int nk = (K + LM_BK - 1) / LM_BK;
+    const int n_mpair = ((M + LM_BM - 1) / LM_BM + 1) / 2;
+    const int n_tiles = n_mpair * ((N + LM_BN - 1) / LM_BN);
+    const int cid = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
+    const volatile int* vfailed = &failed;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -117,87 +169,125 @@ __global__ void __launch_bounds__(128, 1)
     if (threadIdx.x == 32) {
         for (int s = 0; s < LM_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);  // one commit from each CTA's MMA issuer
         }
-        mbar_init(&done, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 4);  // lane 0 of each epilogue warp
+        }
         failed = 0;
         fence_barrier_init();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the peer's barriers are initialised before any copy or commit reaches them
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
     if (threadIdx.x == 0) {
         // ---------------- producer: K slices of H and W into the ring
-        for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % LM_STAGES;
-            if (kt >= LM_STAGES && !mbar_wait(&empty[s], ((kt / LM_STAGES) - 1) & 1)) {
+        uint32_t it = 0;
+        for (int t = cid; t < n_tiles && !*vfailed; t += n_cl) {
+            const int m0 = ((t % n_mpair) * 2 + (int)rank) * LM_BM;
+            const int n0 = (t / n_mpair) * LM_BN;
+            for (int kt = 0; kt < nk; ++kt, ++it) {
+                const uint32_t s = it % LM_STAGES;
+                if (it >= LM_STAGES && !lm_wait(&empty[s], ((it / LM_STAGES) - 1) & 1, vfailed)) {
+                    failed = 1;
+                    break;
+                }
+                unsigned char* a = base + s * LM_STAGE_BYTES;
+                unsigned char* b = a + LM_A_BYTES;
+                mbar_arrive_expect_tx(&full[s], LM_STAGE_BYTES);
+                tma_load_2d(a, &tmap_h, kt * LM_BK, m0, &full[s]);
+#pragma unroll
+                for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)
+                    tma_load_2d_mc(b + j * LM_BOX_B, &tmap_w, n0 + 64 * j, kt * LM_BK, &full[s], 0x3);
+            }
+        }
+        // drain: every stage this CTA filled has been read by both MMAs, so
+        // no commit of the peer is still on its way to this CTA's barriers
+        for (uint32_t i = it; i < it + LM_STAGES && !*vfailed; ++i)
+            if (i >= LM_STAGES && !lm_wait(&empty[i % LM_STAGES], ((i / LM_STAGES) - 1) & 1, vfailed))
+                failed = 1;
+    } else if (threadIdx.x == 32) {
+        // ---------------- MMA issuer
+        uint32_t it = 0, ti = 0;
+        for (int t = cid; t < n_tiles && !*vfailed; t += n_cl, ++ti) {
+            const uint32_t acc = ti & 1;
+            if (ti >= 2 && !lm_wait(&acc_empty[acc], ((ti >> 1) - 1) & 1, vfailed)) {
                 failed = 1;
                 break;
             }
-            unsigned char* a = base + s * LM_STAGE_BYTES;
-            unsigned char* b = a + LM_A_BYTES;
-            mbar_arrive_expect_tx(&full[s], LM_STAGE_BYTES);
-            tma_load_2d(a, &tmap_h, kt * LM_BK, m0, &full[s]);
+            tc_fence_after();
+            const uint32_t d = tmem + acc * LM_ACC_COLS;
+            for (int kt = 0; kt < nk; ++kt, ++it) {
+                const uint32_t s = it % LM_STAGES;
+                if (!lm_wait(&full[s], (it / LM_STAGES) & 1, vfailed)) {
+                    failed = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = smem_u32(base + s * LM_STAGE_BYTES);
+                const uint32_t b = a + LM_A_BYTES;
 #pragma unroll
-            for (int j = 0; j < LM_BN / 64; ++j)
-                tma_load_2d(b + j * LM_BOX_B, &tmap_w, n0 + 64 * j, kt * LM_BK, &full[s]);
+                for (int kk = 0; kk < LM_BK / 16; ++kk) {
+                    // A: 16 K-elements = 32 bytes along the swizzled row; 8-row
+                    // groups 1024 bytes apart.  B: 16 K-rows = 2048 bytes;
+                    // 64-column boxes 8 KB apart, 8-row groups 1024 bytes apart.
+                    const uint64_t ad = lm_sdesc(a + kk * 32, 16, 1024);
+                    const uint64_t bd = lm_sdesc(b + kk * 2048, LM_BOX_B, 1024);
+                    lm_mma(d, ad, bd, (kt | kk) != 0 ? 1u : 0u);
+                }
+                lm_commit_mc(&empty[s], 0x3);  // the stage is free in both CTAs once read
+            }
+            lm_commit(&acc_full[acc]);  // the accumulator is complete (or the loop gave up)
         }
-    } else if (threadIdx.x == 32) {
-        // ---------------- MMA issuer
-        bool ok = true;
-        for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % LM_STAGES;
-            if (!mbar_wait(&full[s], (kt / LM_STAGES) & 1)) {
-                ok = false;
+    } else if (warp >= 2) {
+        // ---------------- epilogue: warp w reads accumulator lanes 32 (w % 4) ..
+        const int q = warp & 3;
+        uint32_t ti = 0;
+        for (int t = cid; t < n_tiles && !*vfailed; t += n_cl, ++ti) {
+            const uint32_t acc = ti & 1;
+            const bool have = __all_sync(0xffffffffu, lm_wait(&acc_full[acc], (ti >> 1) & 1, vfailed));
+            tc_fence_after();
+            if (!have || *vfailed) {
+                if (lane == 0) failed = 1;
                 break;
             }
-            tc_fence_after();
-            const uint32_t a = smem_u32(base + s * LM_STAGE_BYTES);
-            const uint32_t b = a + LM_A_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < LM_BK / 16; ++kk) {
-                // A: 16 K-elements = 32 bytes along the swizzled row; 8-row
-                // groups 1024 bytes apart.  B: 16 K-rows = 2048 bytes; 64-column
-                // boxes 8 KB apart, 8-row groups 1024 bytes apart.
-                const uint64_t ad = lm_sdesc(a + kk * 32, 16, 1024);
-                const uint64_t bd = lm_sdesc(b + kk * 2048, LM_BOX_B, 1024);
-                lm_mma(tmem, ad, bd, (kt | kk) != 0 ? 1u : 0u);
-            }
-            lm_commit(&empty[s]);  // the stage is free once these MMAs have read it
-        }
-        if (!ok) failed = 1;
-        lm_commit(&done);  // the accumulator is complete (or the loop gave up)
-    }
-    // ---------------- epilogue: one accumulator row per thread
-    const bool have = __all_sync(0xffffffffu, mbar_wait(&done, 0));
-    tc_fence_after();
-    if (have && !*(volatile int*)&failed) {
-        const int row = m0 + warp * 32 + lane;
+            const int m0 = ((t % n_mpair) * 2 + (int)rank) * LM_BM;
+            const int n0 = (t / n_mpair) * LM_BN;
+            const int row = m0 + q * 32 + lane;
+            const uint32_t src = tmem + acc * LM_ACC_COLS + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-        for (int c = 0; c < LM_BN; c += 32) {
-            uint32_t v[32];
-            lm_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-            if (row < M) {
-                float* o = out + (int64_t)row * ldo + n0 + c;
-                const int nvalid = min(32, N - (n0 + c));
-                if (nvalid == 32) {
+            for (int c = 0; c < LM_BN; c += 32) {
+                uint32_t v[32];
+                lm_ld32(src + (uint32_t)c, v);
+                if (row < M) {
+                    float* o = out + (int64_t)row * ldo + n0 + c;
+                    const int nvalid = min(32, N - (n0 + c));
+                    if (nvalid == 32) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        reinterpret_cast<float4*>(o)[q] =
-                            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                } else {
-                    for (int q = 0; q < nvalid; ++q) o[q] = __uint_as_float(v[q]);
+                        for (int g = 0; g < 8; ++g)
+                            reinterpret_cast<float4*>(o)[g] =
+                                make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                            __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < 32; ++g)
+                            if (g < nvalid) o[g] = __uint_as_float(v[g]);
+                    }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
-    } else if (threadIdx.x == 0 && err) {
-        atomicOr(err, 8u);  // a bounded wait ran out: the tile was not written
     }
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0 && failed && err) atomicOr(err, 8u);  // a bounded wait ran out
+    cluster_sync();  // neither CTA leaves while the other may still reach its memory
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LM_TMEM_COLS)
                      : "memory");
@@ -252,18 +342,39 @@ bool lmhead_shape_ok(const void* hidden, const void* w, int M, int N, int K)
 cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, int N, int K, int64_t ldo,
                           unsigned* err, cudaStream_t s)
 {
-    static bool attr = false;
-    if (!attr) {
+    static int max_clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(LM_THREADS);
+    cfg.dynamicSmemBytes = LM_SMEM;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (max_clusters == 0) {
         cudaError_t e = cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, LM_SMEM);
         if (e != cudaSuccess) return e;
-        attr = true;
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        cfg.gridDim = dim3((unsigned)(sms & ~1));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_lmhead, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = sms / 2;
+        }
+        max_clusters = n;
     }
     CUtensorMap mh, mw;
     if (!bf16_map(&mh, hidden, M, K, LM_BK, LM_BM) || !bf16_map(&mw, w, K, N, 64, LM_BK))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((N + LM_BN - 1) / LM_BN), (unsigned)((M + LM_BM - 1) / LM_BM));
-    k_lmhead<<<grid, 128, LM_SMEM, s>>>(mh, mw, out, M, N, K, ldo, err);
-    return cudaGetLastError();
+    const int n_mpair = ((M + LM_BM - 1) / LM_BM + 1) / 2;
+    const int n_tiles = n_mpair * ((N + LM_BN - 1) / LM_BN);
+    cfg.gridDim = dim3((unsigned)(2 * std::min(n_tiles, max_clusters)));
+    return cudaLaunchKernelEx(&cfg, k_lmhead, mh, mw, out, M, N, K, ldo, err);
 }
 
 }  // namespace sv
