@@ -56,7 +56,7 @@ def _stage1_kernel(w) -> str:
     row_bytes = w.V * (2 if w.dtype == "bf16" else 4)
     if row_bytes % 16:
         return "k_rows"
-    return "k_stream_cand" if 1 <= w.top_k <= 128 and w.top_k < w.V else "k_stream"
+    return "k_stream"
 
 
 def _traffic(kernel: str, w):

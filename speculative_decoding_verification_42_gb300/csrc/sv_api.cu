@@ -187,7 +187,7 @@ cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool
 {
     const bool rec = timed && h->prof_begin;
     if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
-    cudaError_t e = p.cand ? launch_stream_cand(p, dtype, h->num_sms, s)
+    cudaError_t e = p.cand && !p.gather ? launch_stream_cand(p, dtype, h->num_sms, s)
                   : vec    ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
                            : launch_rows(p, dtype, false, s);
     if (e != cudaSuccess) return e;
@@ -338,6 +338,7 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     p.npiece = (int)cdiv((int64_t)p.V * elem_size(dtype), CS_PIECE);
     p.cand = vec && h->cand_rows && p.seg_mode == SEG_CHUNK && warp_merge_ok(p) &&
              p.top_k >= 1 && p.top_k <= CAND_TOPK_MAX;
+    p.gather = p.cand ? 1 : 0;
 
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;

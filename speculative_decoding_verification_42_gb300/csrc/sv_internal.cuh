@@ -126,6 +126,7 @@ struct Params {
     // top-k candidates written while a piece of a row is in shared memory
     int32_t cand;             // 1: the candidate stream kernel runs (top-k <= CAND_TOPK_MAX)
     int32_t npiece;           // pieces (CS_PIECE bytes) per row
+    int32_t gather;           // top-k rows: the merge gathers candidates from the chunk keys
     unsigned* rowctl;         // [rows, 4]: candidate count, threshold, largest chunk key, 0
     unsigned long long* cand_rows;  // [rows, RCAP_ROW] candidates (order key << 32 | token id)
     unsigned* seq_done;       // [B] sequences decided inside the merge grid
