@@ -35,8 +35,6 @@ struct spec_verify {
     unsigned long long* grab;
     unsigned* done;
     unsigned* err;
-    unsigned long long* cand_rows;  // NULL: this workspace has no candidate arrays
-    unsigned* rowctl;
     unsigned* seq_done;
     // spec_verify_set_profiling: events around the stage-1 stream kernel and
     // where each run stores the number of kernels it launched (all optional)
@@ -106,15 +104,12 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.grab = h->grab;
     p.done = h->done;
     p.err = h->err;
-    p.rowctl = h->rowctl;
-    p.cand_rows = h->cand_rows;
     p.seq_done = h->seq_done;
 }
 
-// one workspace: 256-byte aligned sub-buffers for max_batch x max_k x vocab;
-// candidate blocks only when with_cand.  Fills h's pointers when base is not
-// NULL; returns the bytes needed.
-size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
+// one workspace: 256-byte aligned sub-buffers for max_batch x max_k x vocab.
+// Fills h's pointers when base is not NULL; returns the bytes needed.
+size_t layout_workspace(spec_verify* h, void* base)
 {
     const spec_verify_config* cfg = &h->cfg;
     const int64_t V = cfg->vocab;
@@ -149,11 +144,9 @@ size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
     const size_t o_done = take(sizeof(unsigned));
     const size_t o_err = take(sizeof(unsigned));
     const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
-    const size_t o_ctl = take(sizeof(unsigned) * 4 * h->rows_cap);
     const bool lmhead = cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
     const size_t o_logits =
         lmhead ? take(sizeof(float) * (size_t)cfg->max_batch * (cfg->max_k + 1) * (size_t)V) : 0;
-    const size_t o_cand = with_cand ? take(sizeof(unsigned long long) * RCAP_ROW * h->rows_cap) : 0;
     if (base) {
         char* b = (char*)base;
         h->ws = base;
@@ -171,9 +164,7 @@ size_t layout_workspace(spec_verify* h, bool with_cand, void* base)
         h->done = (unsigned*)(b + o_done);
         h->err = (unsigned*)(b + o_err);
         h->seq_done = (unsigned*)(b + o_sd);
-        h->rowctl = (unsigned*)(b + o_ctl);
         h->logits = lmhead ? (float*)(b + o_logits) : nullptr;
-        h->cand_rows = with_cand ? (unsigned long long*)(b + o_cand) : nullptr;
     }
     return off;
 }
@@ -187,13 +178,13 @@ cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool
 {
     const bool rec = timed && h->prof_begin;
     if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
-    cudaError_t e = p.cand && !p.gather ? launch_stream_cand(p, dtype, h->num_sms, s)
-                  : vec    ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
-                           : launch_rows(p, dtype, false, s);
+    cudaError_t e = vec ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
+                        : launch_rows(p, dtype, false, s);
     if (e != cudaSuccess) return e;
     if (rec && cudaEventRecord(h->prof_end, s) != cudaSuccess) return cudaErrorUnknown;
-    // the merge grid, then (warp merges) the decision grid
+    // the merge grid, then (warp and top-k merges) the decision grid
     *launches += warp_merge_ok(p) ? 3 : 2;
+    if (p.cand) return launch_merge_topk(p, dtype, s);
     return warp_merge_ok(p) ? launch_merge_warp(p, dtype, s) : launch_merge(p, dtype, s);
 }
 
@@ -268,13 +259,13 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
         delete h;
         return SPEC_ERR_CUDA;
     }
-    layout_workspace(h, true, nullptr);
+    layout_workspace(h, nullptr);
     // stage-1 work items (row slot, segment) are counted in 32-bit ints
     if (h->rows_cap * h->nseg_cap >= (int64_t)INT32_MAX) {
         delete h;
         return SPEC_ERR_INVALID_ARG;
     }
-    h->ws_bytes = layout_workspace(h, true, nullptr);
+    h->ws_bytes = layout_workspace(h, nullptr);
     void* base = nullptr;
     if (cudaMalloc(&base, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -286,7 +277,7 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
         delete h;
         return SPEC_ERR_CUDA;
     }
-    layout_workspace(h, true, base);
+    layout_workspace(h, base);
     *out = h;
     return SPEC_OK;
 }
@@ -334,11 +325,9 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     choose_seg_mode(p, dtype);
     const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(p.target) &&
                      (cfg.draft_kind == SPEC_DRAFT_PROBS || aligned16(in->draft));
-    // top-k rows: candidates written while each segment is in shared memory
-    p.npiece = (int)cdiv((int64_t)p.V * elem_size(dtype), CS_PIECE);
-    p.cand = vec && h->cand_rows && p.seg_mode == SEG_CHUNK && warp_merge_ok(p) &&
-             p.top_k >= 1 && p.top_k <= CAND_TOPK_MAX;
-    p.gather = p.cand ? 1 : 0;
+    // top-k rows: the chunks reaching the row's bound gathered by one CTA per row
+    p.cand = vec && p.seg_mode == SEG_CHUNK && warp_merge_ok(p) && p.top_k >= 1 &&
+             p.top_k <= CAND_TOPK_MAX;
 
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
@@ -468,14 +457,10 @@ size_t layout_over(spec_verify* h, const spec_verify_config* cfg, int32_t batch,
     h->cfg = *cfg;
     h->cfg.max_batch = (int32_t)mb;
     h->cfg.max_k = k_max;
-    const size_t need = layout_workspace(h, false, nullptr);
+    const size_t need = layout_workspace(h, nullptr);
     if (h->rows_cap * h->nseg_cap >= (int64_t)INT32_MAX) return 0;
-    // candidate blocks when they fit in what is left of the caller's memory
-    const size_t with_cand = layout_workspace(h, true, nullptr);
-    const bool cand = ws && with_cand <= ws_bytes;
-    const size_t off = cand ? with_cand : need;
-    if (ws) layout_workspace(h, cand, ws);
-    return off;
+    if (ws) layout_workspace(h, ws);
+    return need;
 }
 
 }  // namespace
@@ -505,8 +490,7 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
         cudaMemsetAsync(h.seq_ticket, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h.job_ticket, 0, sizeof(unsigned) * (size_t)h.jobs_cap, cs) != cudaSuccess ||
         cudaMemsetAsync(h.grab, 0, 256 * 3, cs) != cudaSuccess ||
-        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
-        cudaMemsetAsync(h.rowctl, 0, sizeof(unsigned) * 4 * (size_t)h.rows_cap, cs) != cudaSuccess)
+        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return spec_verify_run(&h, in, s, out, stream);
 }

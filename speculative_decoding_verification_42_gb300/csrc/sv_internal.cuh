@@ -123,26 +123,11 @@ struct Params {
     unsigned long long* grab; // streaming kernel: next work item (reset by the last CTA)
     unsigned* done;           // streaming kernel: CTAs finished
     unsigned* err;            // bounded waits that ran out (0 = none)
-    // top-k candidates written while a piece of a row is in shared memory
-    int32_t cand;             // 1: the candidate stream kernel runs (top-k <= CAND_TOPK_MAX)
-    int32_t npiece;           // pieces (CS_PIECE bytes) per row
-    int32_t gather;           // top-k rows: the merge gathers candidates from the chunk keys
-    unsigned* rowctl;         // [rows, 4]: candidate count, threshold, largest chunk key, 0
-    unsigned long long* cand_rows;  // [rows, RCAP_ROW] candidates (order key << 32 | token id)
+    int32_t cand;             // 1: top-k rows (1 <= top-k <= CAND_TOPK_MAX) take k_merge_cand
     unsigned* seq_done;       // [B] sequences decided inside the merge grid
 };
 
-// ------------------------------------------------------------------------- //
-// top-k candidates.  While a piece of a row is in shared memory its warp     //
-// knows a lower bound tau of the row's k-th largest logit: the k-th largest  //
-// of logits it has seen in the row (16-byte word maxima; each is a logit of  //
-// the row, so at least k logits are >= tau).  Every logit >= tau is a        //
-// candidate, so the row's top-k is contained in its candidates.              //
-// ------------------------------------------------------------------------- //
-constexpr int CS_PIECE = 4096;      // bytes of one piece (32 chunks of 128 bytes)
-constexpr int CAND_TOPK_MAX = 128;  // largest top-k the candidate path serves
-constexpr int RCAP_ROW = 2048;      // candidates a row can hold
-enum : int { CTL_COUNT = 0, CTL_TAU = 1, CTL_MAXKEY = 2 };
+constexpr int CAND_TOPK_MAX = 128;  // largest top-k the row merge of sv_mcand.cuh serves
 
 // ------------------------------------------------------------------------- //
 // order keys: unsigned keys whose order is the order of the float values,    //
@@ -538,8 +523,9 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 // launchers (defined in the .cu files)
 cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_t s);
-// the candidate stream kernel (one warp per CTA, as many as fit each SM)
-cudaError_t launch_stream_cand(const Params& p, int dtype, int num_sms, cudaStream_t s);
+// top-k rows: the row merge (one CTA per row) and the decision grid for what
+// it leaves, both programmatic dependents of the stream
+cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s);
 cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);
 cudaError_t launch_merge_warp(const Params& p, int dtype, cudaStream_t s);
 // rows whose merge the warp kernel handles: fast top-k rows, or rows without knobs

@@ -1350,7 +1350,6 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 }  // namespace sv
 
 #include "sv_warp.cuh"
-#include "sv_cand.cuh"
 #include "sv_mcand.cuh"
 
 namespace sv {
@@ -1420,12 +1419,23 @@ static cudaError_t launch_merge_warp_t(const Params& p, cudaStream_t s)
         if (e0 != cudaSuccess) return e0;
         attr = true;
     }
-    cudaError_t e = p.cand ? launch_dependent(k_merge_cand<T>, p, (unsigned)rows, MC_T, 0, s)
-                           : launch_dependent(k_merge_warp<T>, p,
-                                              (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
-                                              WM_WARPS * 32, WM_SMEM, s);
+    cudaError_t e = launch_dependent(k_merge_warp<T>, p, (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
+                                     WM_WARPS * 32, WM_SMEM, s);
     if (e != cudaSuccess) return e;
     return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
+}
+
+template <typename T>
+static cudaError_t launch_merge_topk_t(const Params& p, cudaStream_t s)
+{
+    cudaError_t e = launch_dependent(k_merge_cand<T>, p, (unsigned)(p.B * p.rps), MC_T, 0, s);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
+}
+
+cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s)
+{
+    return dtype == 1 ? launch_merge_topk_t<__nv_bfloat16>(p, s) : launch_merge_topk_t<float>(p, s);
 }
 
 cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s)

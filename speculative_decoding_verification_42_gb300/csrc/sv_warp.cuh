@@ -298,72 +298,6 @@ __device__ bool warp_fast_topk(const Params& p, const T* row, int r, int x, Warp
     return true;
 }
 
-// the candidate words of a row the merge loads before it knows their count:
-// word lane + 32 g of the row's array for g < CAND_PREFETCH (two candidates
-// per 16-byte word)
-constexpr int CAND_PREFETCH = 8;
-
-// the top-k of row r from the candidates the stream kernel collected (a flat
-// array and the row's control words c4, reset here for the next launch;
-// pre: the prefetched words): 1 when st is final, 0 when the chunk-key path
-// has to run instead (candidates were lost, or more pass the row threshold
-// than the warp stages)
-template <typename T>
-__device__ int warp_cand_topk(const Params& p, int r, int x, WarpSmem& ws, RowStat& st, uint4 c4,
-                              const uint4 (&pre)[CAND_PREFETCH])
-{
-    const unsigned FULL = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    if (lane == 0) *reinterpret_cast<uint4*>(p.rowctl + (int64_t)r * 4) = make_uint4(0, 0, 0, 0);
-    const uint32_t cnt = c4.x, tau = c4.y, maxkey = c4.z;
-    if (maxkey >= 0xFF80u || maxkey <= 0x007Fu) {  // NaN or +inf, or no finite logit
-        st.flags = FLAG_NONFINITE;
-        return 1;
-    }
-    if (cnt > (uint32_t)RCAP_ROW || cnt == 0u) return 0;
-    const uint4* src = reinterpret_cast<const uint4*>(p.cand_rows + (int64_t)r * RCAP_ROW);
-    const int nw = (int)((cnt + 1u) / 2u);
-    int n = 0;
-    // the candidates at or above the row threshold are appended with ballots
-    auto append = [&](const uint4& w, int wi) -> bool {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t key = h ? w.w : w.y;
-            const uint32_t id = h ? w.z : w.x;  // ~0: an unused slot
-            const bool take = wi < nw && 2 * wi + h < (int)cnt && id < (uint32_t)p.V && (key >> 16) >= tau;
-            const unsigned bal = __ballot_sync(FULL, take);
-            if (n + __popc(bal) > WM_CAND) return false;
-            if (take) ws.cand[n + __popc(bal & ((1u << lane) - 1u))] = ((unsigned long long)(~key) << 32) | id;
-            n += __popc(bal);
-        }
-        return true;
-    };
-#pragma unroll
-    for (int g = 0; g < CAND_PREFETCH; ++g) {
-        if (g * 32 >= nw) break;  // warp-uniform
-        if (!append(pre[g], g * 32 + lane)) return 0;
-    }
-    // the rest (more than the prefetch), eight loads in flight per lane
-#pragma unroll 1
-    for (int w0 = CAND_PREFETCH * 32; w0 < nw; w0 += 32 * 8) {
-        uint4 w[8];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            const int wi = w0 + g * 32 + lane;
-            w[g] = wi < nw ? __ldcg(src + wi) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            if (w0 + g * 32 >= nw) break;  // warp-uniform
-            if (!append(w[g], w0 + g * 32 + lane)) return 0;
-        }
-    }
-    __syncwarp();
-    if (n < 1) return 0;  // cannot happen for a finite row; the chunk path decides
-    warp_topk_tail(p, r, ws, n, x, st);
-    return 1;
-}
-
 // statistics over all tokens (no knobs) from the segment records, by one warp
 __device__ __forceinline__ void warp_all_stats(const Params& p, int r, RowStat& st)
 {
@@ -397,17 +331,18 @@ __device__ __forceinline__ void warp_all_stats(const Params& p, int r, RowStat& 
 // ------------------------------------------------------------------------- //
 template <typename T>
 __device__ int warp_sample_list(const Params& p, int tr, const RowStat& ts, bool residual,
-                                const DraftRef& d, float u, WarpSmem& ws,
+                                const DraftRef& d, float u, unsigned char* stage,
                                 unsigned long long* Zfix, bool* zero)
 {
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int n = ts.n_kept;  // <= WM_CAND in the warp path
-    int32_t* ti = reinterpret_cast<int32_t*>(ws.keys);
-    float* tv = reinterpret_cast<float*>(ws.keys) + WM_CAND;
-    int32_t* di = reinterpret_cast<int32_t*>(ws.keys) + 2 * WM_CAND;
-    float* dv = reinterpret_cast<float*>(ws.keys) + 3 * WM_CAND;
-    static_assert(4 * WM_CAND * 4 <= (int)sizeof(ws.keys), "two staged lists fit the key staging");
+    // stage: 4 WM_CAND words (16-byte aligned) for the two lists
+    int32_t* ti = reinterpret_cast<int32_t*>(stage);
+    float* tv = reinterpret_cast<float*>(stage) + WM_CAND;
+    int32_t* di = reinterpret_cast<int32_t*>(stage) + 2 * WM_CAND;
+    float* dv = reinterpret_cast<float*>(stage) + 3 * WM_CAND;
+    static_assert(4 * WM_CAND * 4 <= (int)sizeof(WarpSmem::keys), "two staged lists fit the key staging");
     StagedList tl{ti, tv, n}, dl{di, dv, 0};
     {
         const int32_t* gi = p.kept_id + (int64_t)tr * KCAP;
@@ -511,7 +446,7 @@ __device__ __forceinline__ RowStat rec_stat(const RecWords& w)
 // draft rows 0..K_b-1) and slot i's drafted token, all loaded in one round;
 // the same arithmetic and outputs as warp_decide
 template <typename T>
-__device__ bool warp_decide_lanes(const Params& p, int b, int kb, WarpSmem& ws)
+__device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char* stage)
 {
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -594,7 +529,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, WarpSmem& ws)
     if (ts.mode == MODE_LIST) {
         unsigned long long Z;
         bool zero;
-        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, ws, &Z, &zero);
+        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, stage, &Z, &zero);
         if (lane == 0) {
             p.tokens[(int64_t)b * (K + 1) + jstar] = tok;
             p.num_accepted[b] = jstar;
@@ -622,7 +557,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, WarpSmem& ws)
 // true when the warp decided sequence b; false leaves it to the decision grid
 // (a row of it needs the block merge)
 template <typename T>
-__device__ bool warp_decide(const Params& p, int b, WarpSmem& ws)
+__device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
 {
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -718,7 +653,7 @@ __device__ bool warp_decide(const Params& p, int b, WarpSmem& ws)
     if (ts.mode == MODE_LIST) {
         unsigned long long Z;
         bool zero;
-        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, ws, &Z, &zero);
+        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, stage, &Z, &zero);
         if (lane == 0) {
             p.tokens[(int64_t)b * (K + 1) + jstar] = tok;
             p.num_accepted[b] = jstar;
@@ -759,19 +694,10 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     const int r = blockIdx.x * WM_WARPS + warp;
     if (r >= p.B * p.rps) return;
     // every load that does not depend on another goes out at once: the
-    // sequence's K_b, the row's drafted token, its control words and the
-    // first candidate words
+    // sequence's K_b and the row's drafted token
     const int b = r / p.rps, slot = r - b * p.rps;
     const int jd = slot > p.Kmax ? slot - (p.Kmax + 1) : slot;  // position of the row
     const int x_raw = jd < p.Kmax ? __ldg(p.xin + (int64_t)b * p.Kmax + jd) : -1;
-    uint4 c4 = make_uint4(0, 0, 0, 0);
-    uint4 pre[CAND_PREFETCH];
-    if (p.cand) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.cand_rows + (int64_t)r * RCAP_ROW);
-        c4 = __ldcg(reinterpret_cast<const uint4*>(p.rowctl + (int64_t)r * 4));
-#pragma unroll
-        for (int g = 0; g < CAND_PREFETCH; ++g) pre[g] = __ldcg(src + g * 32 + lane);
-    }
     const RowRef rr = row_ref(p, r);
     if (!rr.valid) {
         if (lane == 0) report_skipped_row(p, rr);
@@ -794,8 +720,7 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     st.px = 0.f;
     st.pad[0] = st.pad[1] = st.pad[2] = 0;
     if (p.seg_mode == SEG_CHUNK) {
-        const int done = p.cand ? warp_cand_topk<T>(p, r, x, ws, st, c4, pre) : 0;
-        if (!done && !warp_fast_topk<T>(p, row, r, x, ws, st)) st.flags |= FLAG_BLOCK_MERGE;
+        if (!warp_fast_topk<T>(p, row, r, x, ws, st)) st.flags |= FLAG_BLOCK_MERGE;
     } else {
         warp_all_stats(p, r, st);
         if (!st.flags && x >= 0) st.px = row_prob(p, Elem<T>::load_cg(row, x), st.M, st.S);
@@ -816,7 +741,8 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     if (lane == 0) __threadfence();
     __syncwarp();
     const int nrows_b = p.draft_kind == 0 ? 2 * rr.kb + 1 : rr.kb + 1;
-    if (nrows_b <= 32 ? warp_decide_lanes<T>(p, rr.b, rr.kb, ws) : warp_decide<T>(p, rr.b, ws)) {
+    unsigned char* stage = reinterpret_cast<unsigned char*>(ws.keys);
+    if (nrows_b <= 32 ? warp_decide_lanes<T>(p, rr.b, rr.kb, stage) : warp_decide<T>(p, rr.b, stage)) {
         __syncwarp();
         if (lane == 0) p.seq_done[rr.b] = 1u;
     }
