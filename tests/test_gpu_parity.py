@@ -79,13 +79,13 @@ def test_several_segments(orc, V, dtype, knobs):
     _check(orc, w)
 
 
-# ----------------------------------------------- top-k candidate stream --
-# Top-k rows (k <= 128, 16-byte rows) take the stream kernel that writes the
-# logits at or above a running top-k bound while each segment is in shared
-# memory.  Its warps own runs of consecutive segments, so the bound carries
-# across the segments of a row once a batch has more segments than the grid
-# has warps (these sizes do); a segment with fewer than k chunks uses its
-# 16-byte word maxima; an overflowing segment sends the row to the chunk path.
+# ------------------------------------------------------- top-k row merge --
+# Top-k rows (k <= 128, 16-byte rows) are streamed for their 16-bit chunk
+# keys, then one CTA per row takes the k-th largest chunk key as the bound,
+# re-reads the chunks reaching it and ranks their logits exactly; rows with
+# more candidates than the CTA stages (ties) go to the decision grid's block
+# merge.  f32 rows have 32-element chunks; the last chunk of a row may be
+# short.
 @pytest.mark.parametrize("V,dtype,B,K,knobs", [
     (128256, "bf16", 16, 8, dict(top_k=50, temperature=0.7)),
     (128256, "f32", 8, 8, dict(top_k=50)),                  # last segment: 40 chunks < k
@@ -93,7 +93,7 @@ def test_several_segments(orc, V, dtype, knobs):
     (65536, "bf16", 16, 4, dict(top_k=1, temperature=1.5)),
     (40000, "f32", 24, 5, dict(top_k=7, temperature=0.5)),
 ])
-def test_candidate_stream(orc, V, dtype, B, K, knobs):
+def test_topk_merge(orc, V, dtype, B, K, knobs):
     w = make_workload(f"cand V={V}", B=B, K_max=K, V=V, dtype=dtype, target_std=3.0, peaks=20,
                       peak_height=8.0, draft_noise_std=1.0, ragged_k=(0, K), seed=V + B,
                       **knobs)
@@ -109,10 +109,10 @@ def test_long_drafts(orc):
     _check(orc, w)
 
 
-def test_candidate_stream_heavy_ties(orc):
-    """Logits rounded to integers: many logits tie at the bound, so some
-    segments overflow their candidate block and those rows take the chunk
-    path; ties keep the lowest ids either way."""
+def test_topk_merge_heavy_ties(orc):
+    """Logits rounded to integers: many chunks and logits tie at the bound,
+    so rows overflow the CTA's staging and take the block merge; ties keep
+    the lowest ids either way."""
     from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
     w = make_workload("ties-int", B=8, K_max=4, V=50000, dtype="bf16", target_std=1.5,
                       draft_noise_std=0.7, seed=41, top_k=60)
@@ -121,8 +121,17 @@ def test_candidate_stream_heavy_ties(orc):
     _check(orc, w)
 
 
-def test_candidate_stream_draft_probs(orc):
-    """Top-k target rows through the candidate stream, draft given as f32
+def test_topk_merge_spike(orc):
+    """A few logits far above the rest: the largest chunk key is more than
+    the histogram window above the k-th, so the bound falls back to the first
+    (thread-maximum) bound or to every chunk; the result is the same."""
+    w = make_workload("spike", B=6, K_max=3, V=32768, dtype="bf16", target_std=2.0,
+                      peaks=3, peak_height=3000.0, draft_noise_std=0.5, seed=77, top_k=40)
+    _check(orc, w)
+
+
+def test_topk_merge_draft_probs(orc):
+    """Top-k target rows through the row merge, draft given as f32
     probabilities (not streamed)."""
     w = make_workload("cand-probs", B=10, K_max=5, V=40960, dtype="f32", ragged_k=(0, 5),
                       seed=52, temperature=0.9, top_k=20)
