@@ -25,6 +25,15 @@
  * The output of a sequence is x_0..x_{j*-1} followed by the sampled token:
  * between 1 and K_b + 1 tokens.
  *
+ * Greedy verify (temperature 0).  The limit T -> 0 of the knobs keeps one
+ * token per row, its argmax (the lowest id among equal maxima); x_j is
+ * accepted iff it is the argmax of target row j, and the emitted token is the
+ * argmax of target row j* (or of row K_b when every draft matched): the
+ * greedy ("argmax") decoding that "Speculative Decoding from Scratch", How
+ * much faster in practice? (3.3, 4.1), measures beside temperature 1, taken as
+ * the T -> 0 limit of the acceptance check.  No uniform is drawn, no draft row
+ * is read (draft may be NULL), and top_k / top_p have no effect.
+ *
  * Uniforms.  Philox4x32-10 (Salmon et al., SC'11) keyed by the 64-bit seed;
  * counter = ((j << 2) | tag, b, round_lo, round_hi); u = (word >> 8) * 2^-24.
  * Tag 0: word 0 is the accept uniform of slot j, word 1 the sampling uniform
@@ -102,7 +111,7 @@ typedef struct {
 } spec_verify_config;
 
 typedef struct {
-    float temperature; /* T > 0.  T == 0 (greedy) returns SPEC_ERR_UNSUPPORTED       */
+    float temperature; /* T > 0, or T == 0 for greedy verify (see above)            */
     int32_t top_k;     /* 0 or >= V: off; else keep the k highest logits, ties to   */
                        /* the lower token id                                         */
     float top_p;       /* >= 1: off; in (0, 1): keep the rank-ordered prefix whose   */
@@ -128,10 +137,12 @@ typedef struct {
     int32_t* num_accepted;  /* [B] accepted drafts j* (required); emitted = j* + 1     */
     int32_t* row_status;    /* [B] SPEC_ROW_* or NULL                                 */
     float* p_t_at_draft;    /* [B, k_max] p_t(x_j) after knobs, NaN for j >= K_b; or NULL */
-    float* p_d_at_draft;    /* [B, k_max] p_d(x_j), NaN for j >= K_b; or NULL          */
-    float* residual_mass;   /* [B] sum of max(0, p_t - p_d) at j*, 0 if all accepted; or NULL */
+                            /* (greedy: 1 where x_j is the argmax, else 0)             */
+    float* p_d_at_draft;    /* [B, k_max] p_d(x_j), NaN for j >= K_b (and greedy); or NULL */
+    float* residual_mass;   /* [B] sum of max(0, p_t - p_d) at j*, 0 if all accepted   */
+                            /* (and greedy); or NULL                                   */
     float* target_lse;      /* [B, k_max+1] log-sum-exp of l/T over the kept set, NaN  */
-                            /* beyond K_b; or NULL                                     */
+                            /* beyond K_b (and greedy); or NULL                        */
 } spec_verify_outputs;
 
 /* Allocate a handle and its device workspace on cfg->device (with the LM

@@ -301,6 +301,53 @@ static int probs_row_ok(const double* P, int32_t V)
     return 1;
 }
 
+/* Greedy verify (temperature 0): the limit T -> 0 of the knobs keeps only a
+ * row's argmax, so the acceptance check p_t(x)/p_d(x) > u passes iff x is the
+ * target's argmax, and the token after the accepted prefix is the argmax of
+ * the target row there ("Speculative Decoding from Scratch", How much faster
+ * in practice? (3.3, 4.1): "argmax" decoding).  The lowest id wins a tie, as
+ * in top-k.  Returns -1 for a row the step refuses (NaN, +inf, no finite). */
+static int32_t row_argmax(const double* l, int32_t V)
+{
+    int32_t a = -1;
+    for (int32_t v = 0; v < V; ++v) {
+        if (isnan(l[v]) || l[v] == INFINITY) return -1;
+        if (isfinite(l[v]) && (a < 0 || l[v] > l[a])) a = v;
+    }
+    return a;
+}
+
+static void verify_greedy_seq(const orc_verify_in* in, orc_verify_out* out, int32_t b, int32_t Kb,
+                              double* lrow)
+{
+    const int32_t V = in->V, Kmax = in->K_max;
+    int32_t jstar = -1, tok = -1;
+    for (int32_t j = 0; j <= Kb; ++j) {
+        load_row(in->target, in->target_dtype, (int64_t)b * (Kmax + 1) + j, V, lrow);
+        const int32_t a = row_argmax(lrow, V);
+        if (a < 0) {
+            put_i(out->row_status, b, ORC_ROW_NONFINITE);
+            for (int32_t i = 0; i < Kmax; ++i) put_d(out->p_t_at_draft, (int64_t)b * Kmax + i, NAN);
+            return;
+        }
+        if (j < Kb) {
+            const int32_t x = in->draft_tokens[(int64_t)b * Kmax + j];
+            put_d(out->p_t_at_draft, (int64_t)b * Kmax + j, x == a ? 1.0 : 0.0);
+            if (jstar < 0 && x != a) {
+                jstar = j;
+                tok = a;
+            }
+        } else if (jstar < 0) {
+            jstar = Kb;
+            tok = a;
+        }
+    }
+    for (int32_t j = 0; j < jstar; ++j)
+        put_i(out->tokens, (int64_t)b * (Kmax + 1) + j, in->draft_tokens[(int64_t)b * Kmax + j]);
+    put_i(out->tokens, (int64_t)b * (Kmax + 1) + jstar, tok);
+    put_i(out->num_accepted, b, jstar);
+}
+
 int orc_verify(const orc_verify_in* in, const orc_sampling* s, orc_verify_out* out,
                int32_t b_begin, int32_t b_end)
 {
@@ -346,6 +393,10 @@ int orc_verify(const orc_verify_in* in, const orc_sampling* s, orc_verify_out* o
         }
         if (bad_token) {
             put_i(out->row_status, b, ORC_ROW_BAD_TOKEN);
+            continue;
+        }
+        if (s->temperature == 0.0) {
+            verify_greedy_seq(in, out, b, Kb, lrow);
             continue;
         }
 
@@ -492,6 +543,12 @@ int orc_draft_sample(const orc_verify_in* in, const orc_sampling* s, int32_t* to
             if (margin) margin[drow] = INFINITY;
             if (Kb < 0 || Kb > Kmax || j >= Kb) continue;
             int ok;
+            if (in->draft_kind == ORC_DRAFT_LOGITS && s->temperature == 0.0) {
+                /* greedy drafting: the draft row's argmax (lowest id on ties) */
+                load_row(in->draft, in->draft_dtype, drow, V, lrow);
+                tokens[drow] = row_argmax(lrow, V);
+                continue;
+            }
             if (in->draft_kind == ORC_DRAFT_LOGITS) {
                 load_row(in->draft, in->draft_dtype, drow, V, lrow);
                 ok = orc_row_dist(lrow, V, s->temperature, s->top_k, s->top_p, P, NULL) == 0;

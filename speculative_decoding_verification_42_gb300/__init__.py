@@ -234,8 +234,8 @@ class Verifier:
         the [H, V] matrix."""
         import torch
         if w_vocab is not None:
-            B, K = draft.shape[0], draft.shape[1]
-            V = draft.shape[2]
+            B, K = draft_tokens.shape[0], draft_tokens.shape[1]
+            V = w_vocab.shape[1]
         else:
             B, K1, V = target.shape
             K = K1 - 1

@@ -73,15 +73,18 @@ spec_status fill_knobs(const spec_verify* h, const spec_sampling* s, Params& p)
     if (!s || s->reserved != 0) return SPEC_ERR_INVALID_ARG;
     const float T = s->temperature;
     if (!(T >= 0.f) || isinf(T)) return SPEC_ERR_INVALID_ARG;
-    if (T == 0.f) return SPEC_ERR_UNSUPPORTED;  // greedy verify is a separate mode
     if (s->top_k < 0) return SPEC_ERR_INVALID_ARG;
     if (!(s->top_p > 0.f)) return SPEC_ERR_INVALID_ARG;  // also rejects NaN
     const int V = h->cfg.vocab;
-    p.T = T;
-    p.c = (float)(1.4426950408889634 / (double)T);
-    p.top_k = (s->top_k > 0 && s->top_k < V) ? s->top_k : 0;
-    p.top_p = s->top_p < 1.f ? s->top_p : 1.f;
-    p.top_p_fix = s->top_p < 1.f ? (uint64_t)((double)s->top_p * 72057594037927936.0) : 0;
+    // temperature 0 is greedy: the kept set of every row is its argmax (the
+    // lowest id among equal maxima), i.e. top-k = 1; top-k and top-p do not
+    // change it; the verify reads no draft row
+    p.greedy = T == 0.f ? 1 : 0;
+    p.T = p.greedy ? 1.f : T;
+    p.c = (float)(1.4426950408889634 / (double)p.T);
+    p.top_k = p.greedy ? (V > 1 ? 1 : 0) : (s->top_k > 0 && s->top_k < V) ? s->top_k : 0;
+    p.top_p = p.greedy ? 1.f : s->top_p < 1.f ? s->top_p : 1.f;
+    p.top_p_fix = !p.greedy && s->top_p < 1.f ? (uint64_t)((double)s->top_p * 72057594037927936.0) : 0;
     p.seed = s->seed;
     p.round = s->round;
     return SPEC_OK;
@@ -294,7 +297,8 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     spec_status st = fill_knobs(h, s, p);
     if (st != SPEC_OK) return st;
     if (in->batch == 0) return SPEC_OK;
-    if (!in->target || !in->draft || !out->tokens || !out->num_accepted) return SPEC_ERR_INVALID_ARG;
+    if (!in->target || (!in->draft && !p.greedy) || !out->tokens || !out->num_accepted)
+        return SPEC_ERR_INVALID_ARG;
     if (in->k_max > 0 && !in->draft_tokens) return SPEC_ERR_INVALID_ARG;
     const bool lmhead = cfg.target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
     const int m_rows = in->batch * (in->k_max + 1);  // verified positions (LM-head rows)
@@ -372,6 +376,7 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
     p.rps = k_max;
     p.draft_launch = 1;
     p.draft_kind = 0;
+    p.greedy = 0;  // temperature 0 samples the argmax through the top-1 list
     p.target = nullptr;
     p.draft = draft;
     p.kpr = k_per_row;

@@ -86,6 +86,7 @@ struct Params {
     int32_t chunk_stride; // chunk keys per row in the workspace (multiple of 8)
     int32_t draft_launch; // 1: the draft-side sampler (rows are draft rows only)
     int32_t draft_kind;   // 0 logits, 1 probabilities (float)
+    int32_t greedy;       // temperature 0: accept while x_j is the target's argmax; no draft row read
     int32_t seg_mode;     // SegMode of this launch
     // knobs
     float T;              // temperature
@@ -529,6 +530,17 @@ cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s);
 cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);
 cudaError_t launch_merge_warp(const Params& p, int dtype, cudaStream_t s);
 // rows whose merge the warp kernel handles: fast top-k rows, or rows without knobs
+// draft rows the verify streams and merges: logits, unless greedy
+__host__ __device__ __forceinline__ bool drafts_streamed(const Params& p)
+{
+    return p.draft_kind == 0 && !p.greedy;
+}
+// rows of sequence b the merge grids count: K_b + 1 target rows (+ K_b drafts)
+__host__ __device__ __forceinline__ int seq_rows(const Params& p, int kb)
+{
+    return drafts_streamed(p) ? 2 * kb + 1 : kb + 1;
+}
+
 __host__ __device__ __forceinline__ bool warp_merge_ok(const Params& p)
 {
     return !p.draft_launch && ((p.seg_mode == SEG_CHUNK && p.top_k <= 256 && p.nchunk <= 4096) ||

@@ -337,14 +337,14 @@ __device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
     ssync();
     if (tid == 0) {
         __threadfence();
-        const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
+        const int nrows = seq_rows(p, rr.kb);
         const bool last = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
         if (last) p.seq_ticket[rr.b] = 0u;
         sm.flag = last;
     }
     ssync();
     const bool last = sm.flag != 0;
-    const int nrows_b = p.draft_kind == 0 ? 2 * rr.kb + 1 : rr.kb + 1;
+    const int nrows_b = seq_rows(p, rr.kb);
     if (last && warp == 0 && nrows_b <= 32) {
         if (lane == 0) __threadfence();
         __syncwarp();
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(MC_T, 8) k_merge_cand(const Params p)
         if (threadIdx.x == 0) report_skipped_row(p, rr);
         return;
     }
-    if (rr.is_draft && p.draft_kind == 1) return;  // probabilities: read only where needed
+    if (rr.is_draft && !drafts_streamed(p)) return;  // probabilities (or greedy): read only where needed
     merge_row_topk<T>(p, r, sm);
 }
 

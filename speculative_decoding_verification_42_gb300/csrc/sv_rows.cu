@@ -971,7 +971,7 @@ __device__ void decide_sequence(const Params& p, int b, unsigned char* scratch)
     const T* target = (const T*)p.target;
     const int64_t trow0 = (int64_t)b * (K + 1) * V;
     const int64_t drow0 = (int64_t)b * K * V;
-    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
+    const int nrows = seq_rows(p, kb);
     if (threadIdx.x == 0) {
         s_jstar = kb;
         s_bad = 0;
@@ -988,7 +988,7 @@ __device__ void decide_sequence(const Params& p, int b, unsigned char* scratch)
         const int x = p.xin[(int64_t)b * K + j];
         if (x < 0 || x >= V) {
             s_bad = 1;
-        } else if (p.draft_kind == 1) {
+        } else if (p.draft_kind == 1 && !p.greedy) {
             const float q = __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x);
             if (!(q >= 0.f) || q == INFINITY) s_nonfinite = 1;
         }
@@ -1018,8 +1018,9 @@ __device__ void decide_sequence(const Params& p, int b, unsigned char* scratch)
         const RowStat ts = rs[j];
         bool kt, kd = true;
         const float lt = warp_lookup<T>(p, target_slot(p, b, j), ts, target + trow0 + (int64_t)j * V, x, &kt);
-        float pd;
-        if (p.draft_kind == 1) {
+        float pd = NAN;  // greedy: the draft is not read
+        if (p.greedy) {
+        } else if (p.draft_kind == 1) {
             pd = __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x);
         } else {
             const RowStat ds = rs[kb + 1 + j];
@@ -1029,16 +1030,22 @@ __device__ void decide_sequence(const Params& p, int b, unsigned char* scratch)
         }
         const float pt = kt ? (float)((double)exp2f((lt - ts.M) * p.c) / ts.S) : 0.f;
         if (lane == 0) {
-            const uint4 w = slot_words(p, b, j, 0u);
-            const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
-            if (!((double)u24(w.x) < ratio)) atomicMin(&s_jstar, j);
+            bool rej;
+            if (p.greedy) {
+                rej = !(pt > 0.f);  // the kept set is the target's argmax alone
+            } else {
+                const uint4 w = slot_words(p, b, j, 0u);
+                const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
+                rej = !((double)u24(w.x) < ratio);
+            }
+            if (rej) atomicMin(&s_jstar, j);
             if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = pt;
             if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = pd;
         }
     }
     for (int j = threadIdx.x; j <= K; j += NT) {
         if (p.lse) p.lse[(int64_t)b * (K + 1) + j] =
-            j <= kb ? (float)((double)rs[j].M / (double)p.T + log(rs[j].S)) : NAN;
+            j <= kb && !p.greedy ? (float)((double)rs[j].M / (double)p.T + log(rs[j].S)) : NAN;
         if (j >= kb && j < K) {
             if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
             if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = NAN;
@@ -1048,7 +1055,8 @@ __device__ void decide_sequence(const Params& p, int b, unsigned char* scratch)
     const int jstar = s_jstar;
     for (int j = threadIdx.x; j <= K; j += NT)
         p.tokens[(int64_t)b * (K + 1) + j] = (j < jstar) ? p.xin[(int64_t)b * K + j] : -1;
-    const bool residual = jstar < kb;
+    // greedy: the emitted token is the argmax of target row j* (its kept list)
+    const bool residual = jstar < kb && !p.greedy;
     const uint4 w = slot_words(p, b, jstar, 0u);
     const float u = u24(w.y);
     const int tr = target_slot(p, b, jstar);
@@ -1177,7 +1185,7 @@ __device__ void finish_row(const Params& p, int r, const RowRef& rr, const T* ro
     csync();
     if (threadIdx.x == 0) {
         __threadfence();
-        const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
+        const int nrows = seq_rows(p, rr.kb);
         s_last_seq = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
         if (s_last_seq) {
             __threadfence();
@@ -1206,7 +1214,7 @@ __global__ void __launch_bounds__(NT, 4) k_rows(const Params p)
         if (seg == 0 && threadIdx.x == 0) report_skipped_row(p, rr);
         return;
     }
-    if (rr.is_draft && p.draft_kind == 1) return;  // probabilities: read only where needed
+    if (rr.is_draft && !drafts_streamed(p)) return;  // probabilities (or greedy): read only where needed
 
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     const int64_t base = (int64_t)seg * G::SEG;
@@ -1272,7 +1280,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
                 const int r = (int)(item / p.nseg), seg = (int)(item - (int64_t)r * p.nseg);
                 const RowRef rr = row_ref(p, r);
                 if (!rr.valid) continue;
-                if (rr.is_draft && p.draft_kind == 1) continue;
+                if (rr.is_draft && !drafts_streamed(p)) continue;
             }
             const int s = k % NSTAGE;
             if (k >= NSTAGE && !mbar_wait(&ring.empty[s], ((k / NSTAGE) - 1) & 1)) {
@@ -1342,7 +1350,7 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
         if (threadIdx.x == 0) report_skipped_row(p, rr);
         return;
     }
-    if (rr.is_draft && p.draft_kind == 1) return;  // probabilities: read only where needed
+    if (rr.is_draft && !drafts_streamed(p)) return;  // probabilities (or greedy): read only where needed
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     finish_row<T>(p, r, rr, row, smem_scratch);
 }

@@ -451,7 +451,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int K = p.Kmax, V = p.V;
-    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
+    const int nrows = seq_rows(p, kb);
     const int64_t drow0 = (int64_t)b * K * V;
     RecWords rw{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     if (lane < nrows)
@@ -465,7 +465,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
     bool nonf = __any_sync(FULL, mine && (me.flags & FLAG_NONFINITE));
     const bool bad = __any_sync(FULL, lane < kb && (x < 0 || x >= V));
     float q = 1.f;
-    if (!bad && p.draft_kind == 1) {
+    if (!bad && p.draft_kind == 1 && !p.greedy) {
         if (lane < kb) q = __ldcg((const float*)p.draft + drow0 + (int64_t)lane * V + x);
         nonf |= __any_sync(FULL, lane < kb && (!(q >= 0.f) || q == INFINITY));
     }
@@ -493,11 +493,15 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
     bool rej = false;
     if (lane < kb) {
         const float pt = me.px;
-        const float pd = p.draft_kind == 1 ? q : pd_row;
-        // IEEE: pd = 0 gives inf or NaN; rounding the ratio to fp32 moves it
-        // by < 1e-7 relative, inside the near-tie window
-        const float ratio = __fdiv_rn(pt, pd);
-        rej = !(u24(wrd.x) < ratio);
+        const float pd = p.greedy ? NAN : p.draft_kind == 1 ? q : pd_row;
+        if (p.greedy) {
+            rej = !(pt > 0.f);  // the kept set is the target's argmax alone
+        } else {
+            // IEEE: pd = 0 gives inf or NaN; rounding the ratio to fp32 moves
+            // it by < 1e-7 relative, inside the near-tie window
+            const float ratio = __fdiv_rn(pt, pd);
+            rej = !(u24(wrd.x) < ratio);
+        }
         if (p.p_t_at) p.p_t_at[(int64_t)b * K + lane] = pt;
         if (p.p_d_at) p.p_d_at[(int64_t)b * K + lane] = pd;
     }
@@ -506,7 +510,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
     for (int j = lane; j <= K; j += 32) {
         if (p.lse) {
             // lane j holds target row j for j <= kb (kb < 32 here)
-            p.lse[(int64_t)b * (K + 1) + j] = j <= kb ? me.M / p.T + logf((float)me.S) : NAN;
+            p.lse[(int64_t)b * (K + 1) + j] = j <= kb && !p.greedy ? me.M / p.T + logf((float)me.S) : NAN;
         }
         if (j >= kb && j < K) {
             if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = NAN;
@@ -514,7 +518,8 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
         }
         if (j != jstar) p.tokens[(int64_t)b * (K + 1) + j] = j < jstar ? x : -1;
     }
-    const bool residual = jstar < kb;
+    // greedy: the emitted token is the argmax of target row j* (its kept list)
+    const bool residual = jstar < kb && !p.greedy;
     const float u = u24(__shfl_sync(FULL, wrd.y, jstar));
     const int tr = target_slot(p, b, jstar);
     const RowStat ts = rec_stat(shfl_rec(rw, jstar));
@@ -563,7 +568,7 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
     const int lane = threadIdx.x & 31;
     const int K = p.Kmax, V = p.V;
     const int kb = seq_k(p, b);
-    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
+    const int nrows = seq_rows(p, kb);
     const int64_t drow0 = (int64_t)b * K * V;
     bool bad = false, nonf = false, block = false;
     for (int i = lane; i < nrows; i += 32) {
@@ -579,7 +584,7 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
         const int x = p.xin[(int64_t)b * K + j];
         if (x < 0 || x >= V) {
             bad = true;
-        } else if (p.draft_kind == 1) {
+        } else if (p.draft_kind == 1 && !p.greedy) {
             const float q = __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x);
             if (!(q >= 0.f) || q == INFINITY) nonf = true;
         }
@@ -611,12 +616,16 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
         if (j < kb) {
             const int x = p.xin[(int64_t)b * K + j];
             const float pt = __ldcg(&p.rstat[target_slot(p, b, j)].px);
-            const float pd = p.draft_kind == 1
-                                 ? __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x)
-                                 : __ldcg(&p.rstat[draft_slot(p, b, j)].px);
-            const uint4 w = slot_words(p, b, j, 0u);
-            const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
-            rej = !((double)u24(w.x) < ratio);
+            const float pd = p.greedy             ? NAN
+                             : p.draft_kind == 1 ? __ldcg((const float*)p.draft + drow0 + (int64_t)j * V + x)
+                                                 : __ldcg(&p.rstat[draft_slot(p, b, j)].px);
+            if (p.greedy) {
+                rej = !(pt > 0.f);  // the kept set is the target's argmax alone
+            } else {
+                const uint4 w = slot_words(p, b, j, 0u);
+                const double ratio = (double)pt / (double)pd;  // IEEE: pd = 0 gives inf or NaN
+                rej = !((double)u24(w.x) < ratio);
+            }
             if (p.p_t_at) p.p_t_at[(int64_t)b * K + j] = pt;
             if (p.p_d_at) p.p_d_at[(int64_t)b * K + j] = pd;
         }
@@ -626,7 +635,7 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
     for (int j = lane; j <= K; j += 32) {
         if (p.lse) {
             float v = NAN;
-            if (j <= kb) {
+            if (j <= kb && !p.greedy) {
                 const RowStat* rs = p.rstat + target_slot(p, b, j);
                 v = (float)((double)__ldcg(&rs->M) / (double)p.T + log(__ldcg(&rs->S)));
             }
@@ -638,7 +647,8 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
         }
         if (j != jstar) p.tokens[(int64_t)b * (K + 1) + j] = j < jstar ? p.xin[(int64_t)b * K + j] : -1;
     }
-    const bool residual = jstar < kb;
+    // greedy: the emitted token is the argmax of target row j* (its kept list)
+    const bool residual = jstar < kb && !p.greedy;
     const uint4 w = slot_words(p, b, jstar, 0u);
     const float u = u24(w.y);
     const int tr = target_slot(p, b, jstar);
@@ -703,7 +713,7 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
         if (lane == 0) report_skipped_row(p, rr);
         return;
     }
-    if (rr.is_draft && p.draft_kind == 1) return;
+    if (rr.is_draft && !drafts_streamed(p)) return;
     WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_w)[warp];
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     // the drafted token this row's P(x) is needed at (the bonus row has none)
@@ -732,7 +742,7 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     unsigned last = 0;
     if (lane == 0) {
         __threadfence();
-        const int nrows = (rr.kb + 1) + (p.draft_kind == 0 ? rr.kb : 0);
+        const int nrows = seq_rows(p, rr.kb);
         last = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
         if (last) p.seq_ticket[rr.b] = 0u;
     }
@@ -740,7 +750,7 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     if (!last) return;
     if (lane == 0) __threadfence();
     __syncwarp();
-    const int nrows_b = p.draft_kind == 0 ? 2 * rr.kb + 1 : rr.kb + 1;
+    const int nrows_b = seq_rows(p, rr.kb);
     unsigned char* stage = reinterpret_cast<unsigned char*>(ws.keys);
     if (nrows_b <= 32 ? warp_decide_lanes<T>(p, rr.b, rr.kb, stage) : warp_decide<T>(p, rr.b, stage)) {
         __syncwarp();
@@ -768,7 +778,7 @@ __global__ void __launch_bounds__(NT) k_decide(const Params p)
     }
     csync();
     if (s_done) return;
-    const int nrows = p.draft_kind == 0 ? 2 * kb + 1 : kb + 1;
+    const int nrows = seq_rows(p, kb);
     // which rows the warps left to the block code (bitmask, one load round)
     __shared__ unsigned s_flagged[(2 * 255 + 1 + 31) / 32];
     for (int i = threadIdx.x; i < (nrows + 31) / 32; i += NT) s_flagged[i] = 0u;

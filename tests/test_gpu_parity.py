@@ -5,7 +5,7 @@ relative (see parity_util)."""
 import numpy as np
 import pytest
 
-from parity_util import DELTA, compare, oracle_tokens, run_gpu, run_oracle
+from parity_util import DELTA, compare, oracle_tokens, run_gpu, run_oracle, to_device
 from workloads import make_config, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -141,6 +141,69 @@ def test_topk_merge_draft_probs(orc):
             q[b, j] = orc.row_probs(w.draft[b, j], 0.9, 20)[0].astype(np.float32)
     w.draft, w.draft_kind = q, "probs"
     _check(orc, w)
+
+
+# ---------------------------------------------------- greedy verify (T = 0) --
+# Temperature 0: the kept set of a row is its argmax (lowest id on ties); a
+# draft is accepted iff it is the target's argmax, and the emitted token is the
+# target's argmax at the first mismatch (or at K_b).  No draft row is read.
+@pytest.mark.parametrize("V,dtype,B,K,tied", [
+    (128256, "bf16", 16, 8, False),
+    (32000, "f32", 12, 5, True),
+    (1000, "bf16", 24, 6, True),
+    (2, "f32", 8, 3, True),
+    (130, "bf16", 8, 4, False),      # rows not on 16 bytes: the per-segment path
+])
+def test_greedy_verify(orc, V, dtype, B, K, tied):
+    from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
+    w = make_workload(f"greedy V={V}", B=B, K_max=K, V=V, dtype=dtype, target_std=2.0,
+                      draft_scale=1.0, draft_noise_std=0.3, ragged_k=(0, K), seed=V + 7,
+                      temperature=0.0, top_k=5, top_p=0.5)
+    if tied:  # integer logits: equal maxima in most rows
+        if dtype == "bf16":
+            w.target = f32_to_bf16_bits(np.round(bf16_bits_to_f32(w.target)))
+            w.draft = f32_to_bf16_bits(np.round(bf16_bits_to_f32(w.draft)))
+        else:
+            w.target, w.draft = np.round(w.target), np.round(w.draft)
+    toks, _ = oracle_tokens(orc, w)  # the draft's argmax
+    rng = np.random.default_rng(V)
+    flip = rng.random(toks.shape) < 0.15
+    toks = np.where(flip & (toks >= 0), rng.integers(0, V, toks.shape), toks).astype(np.int32)
+    g = run_gpu(w, toks)
+    o = run_oracle(orc, w, toks)
+    assert compare(g, o, w, toks) == 0  # greedy has no near-ties
+    assert (o["num_accepted"] > 0).any() and (o["num_accepted"] < w.k_per_row).any()
+
+
+def test_greedy_without_draft(orc):
+    """Greedy verify reads no draft row: a NULL draft gives the same result."""
+    import torch
+    import speculative_decoding_verification_42_gb300 as sv
+    w = make_workload("greedy no draft", B=6, K_max=4, V=4096, dtype="bf16", seed=5,
+                      temperature=0.0)
+    toks, _ = oracle_tokens(orc, w)
+    ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype="bf16")
+    out = ver.run(to_device(w.target), None, torch.from_numpy(toks).cuda(),
+                  torch.from_numpy(w.k_per_row).cuda(), temperature=0.0)
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+    ver.close()
+    o = run_oracle(orc, w, toks)
+    assert compare(g, o, w, toks) == 0
+
+
+def test_greedy_draft_sampler(orc):
+    """The draft-side sampler at temperature 0 returns each draft row's argmax."""
+    import torch
+    import speculative_decoding_verification_42_gb300 as sv
+    w = make_workload("greedy drafts", B=8, K_max=5, V=20000, dtype="f32", seed=6,
+                      ragged_k=(0, 5), temperature=0.0)
+    ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype="f32")
+    g = ver.draft_sample(to_device(w.draft), torch.from_numpy(w.k_per_row).cuda(),
+                         temperature=0.0).cpu().numpy()
+    ver.close()
+    want, _ = oracle_tokens(orc, w)
+    np.testing.assert_array_equal(g, want)
 
 
 # ------------------------------------------------------ the five workloads --

@@ -41,6 +41,12 @@ MUTATIONS = {
                               "test_oracle_verify.py"),
     "uniform words swapped": ("if (u0) *u0 = orc_u24(w[0]);", "if (u0) *u0 = orc_u24(w[1]);",
                               "test_oracle_verify.py"),
+    "greedy argmax keeps the last maximum": ("if (isfinite(l[v]) && (a < 0 || l[v] > l[a])) a = v;",
+                                             "if (isfinite(l[v]) && (a < 0 || l[v] >= l[a])) a = v;",
+                                             "test_oracle_greedy.py"),
+    "greedy emits the drafted token at the mismatch": ("                tok = a;\n            }\n        } else if",
+                                                       "                tok = x;\n            }\n        } else if",
+                                                       "test_oracle_greedy.py"),
     "resample uniform from another slot": (
         "u_smp_star = u_smp;",
         "verify_uniforms(s->seed, s->round, b, j + 1, 0u, NULL, &u_smp_star);",
