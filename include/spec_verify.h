@@ -143,6 +143,12 @@ typedef struct {
                             /* (and greedy); or NULL                                   */
     float* target_lse;      /* [B, k_max+1] log-sum-exp of l/T over the kept set, NaN  */
                             /* beyond K_b (and greedy); or NULL                        */
+    float* alpha;           /* [B, k_max] acceptance statistic alpha_j = sum_v          */
+                            /* min(p_t(v), p_d(v)) after the knobs ("Speculative       */
+                            /* Decoding from Scratch", The acceptance rate alpha      */
+                            /* decides everything (3.1-3.2)); NaN for j >= K_b, failed */
+                            /* sequences and greedy; or NULL (not computed: one more  */
+                            /* kernel, which re-reads the rows not kept as lists)      */
 } spec_verify_outputs;
 
 /* Allocate a handle and its device workspace on cfg->device (with the LM

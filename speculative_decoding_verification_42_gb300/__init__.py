@@ -54,7 +54,7 @@ class spec_verify_outputs(C.Structure):
     _fields_ = [("tokens", C.c_void_p), ("num_accepted", C.c_void_p),
                 ("row_status", C.c_void_p), ("p_t_at_draft", C.c_void_p),
                 ("p_d_at_draft", C.c_void_p), ("residual_mass", C.c_void_p),
-                ("target_lse", C.c_void_p)]
+                ("target_lse", C.c_void_p), ("alpha", C.c_void_p)]
 
 
 class SpecVerifyError(RuntimeError):
@@ -228,10 +228,10 @@ class Verifier:
 
     def run(self, target, draft, draft_tokens, k_per_row=None, *, temperature=1.0, top_k=0,
             top_p=1.0, seed=0, round=0, out: dict | None = None, debug: bool = True,
-            stream=None, w_vocab=None) -> dict:
+            stream=None, w_vocab=None, alpha: bool = False) -> dict:
         """Verify a batch; returns (and fills) a dict of output tensors.  With the
         LM head, ``target`` is the hidden states [B * (K + 1), H] and ``w_vocab``
-        the [H, V] matrix."""
+        the [H, V] matrix.  alpha: also the acceptance statistic of every slot."""
         import torch
         if w_vocab is not None:
             B, K = draft_tokens.shape[0], draft_tokens.shape[1]
@@ -250,6 +250,8 @@ class Verifier:
                            residual_mass=torch.empty(B, dtype=torch.float32, device=dev),
                            target_lse=torch.empty((B, K + 1), dtype=torch.float32,
                                                   device=dev))
+            if alpha:
+                out.update(alpha=torch.empty((B, K), dtype=torch.float32, device=dev))
         ins = spec_verify_inputs(_ptr(target), _ptr(w_vocab), _ptr(draft), _ptr(draft_tokens),
                                  _ptr(k_per_row), B, K)
         outs = spec_verify_outputs(*[_ptr(out.get(f)) for f, _ in spec_verify_outputs._fields_])

@@ -323,6 +323,7 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     p.p_d_at = out->p_d_at_draft;
     p.resid_mass = out->residual_mass;
     p.lse = out->target_lse;
+    p.alpha = out->alpha;
     p.probs_out = nullptr;
     fill_workspace(h, p);
     const int dtype = lmhead ? SPEC_F32 : cfg.target_dtype;
@@ -349,6 +350,10 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead) != cudaSuccess) return SPEC_ERR_CUDA;
     if (!all_lists(p)) {
         if (launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        ++launches;
+    }
+    if (p.alpha) {
+        if (launch_alpha(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;
     }
     if (h->prof_launches) *h->prof_launches = launches;

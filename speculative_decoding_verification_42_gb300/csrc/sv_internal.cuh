@@ -108,6 +108,7 @@ struct Params {
     float* p_d_at;            // [B, Kmax] or NULL
     float* resid_mass;        // [B] or NULL
     float* lse;               // [B, Kmax+1] or NULL
+    float* alpha;             // [B, Kmax] acceptance statistic per slot, or NULL
     float* probs_out;         // draft launch: dense [B, Kmax, V] or NULL
     // workspace
     SegStat* seg;             // [rows, nseg]
@@ -547,6 +548,8 @@ __host__ __device__ __forceinline__ bool warp_merge_ok(const Params& p)
                                (p.seg_mode == SEG_SUM && p.top_k == 0 && !(p.top_p < 1.0f)));
 }
 cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s);
+// alpha_j = sum_v min(p_t, p_d) of every slot (when p.alpha is set)
+cudaError_t launch_alpha(const Params& p, int dtype, cudaStream_t s);
 // the LM head: out[M, N] (row stride ldo) = hidden[M, K] x w[K, N], bf16 in, fp32 out
 bool lmhead_shape_ok(const void* hidden, const void* w, int M, int N, int K);
 cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, int N, int K, int64_t ldo,

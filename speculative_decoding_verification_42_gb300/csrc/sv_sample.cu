@@ -251,6 +251,90 @@ __global__ void __launch_bounds__(NT) k_probs(const Params p)
     }
 }
 
+// ------------------------------------------------------------------------- //
+// k_alpha: the acceptance statistic alpha_j = sum_v min(p_t(v), p_d(v)) of   //
+// every drafted slot ("Speculative Decoding from Scratch", The acceptance     //
+// rate alpha decides everything (3.1-3.2)), on request: one CTA per slot,    //
+// summed exactly in 2^-56 fixed point.  A row kept as a list contributes     //
+// only its list; otherwise the pass covers the vocabulary.  NaN where the    //
+// slot is beyond K_b, the sequence failed, or the verify is greedy.          //
+// ------------------------------------------------------------------------- //
+template <typename T>
+__global__ void __launch_bounds__(NT) k_alpha(const Params p)
+{
+    __shared__ unsigned long long s_red[NT / 32 + 1];
+    const int K = p.Kmax;
+    const int b = blockIdx.x / K, j = blockIdx.x - b * K;
+    const int kb = seq_k(p, b);
+    float* dst = p.alpha + (int64_t)b * K + j;
+    if (!k_ok(p, kb) || j >= kb || p.greedy || __ldcg(p.num_accepted + b) < 0) {
+        if (threadIdx.x == 0) *dst = NAN;
+        return;
+    }
+    const float c = p.c;
+    const int V = p.V;
+    const int tr = target_slot(p, b, j);
+    const RowStat ts = load_rowstat(p.rstat + tr);
+    const T* trow = (const T*)p.target + ((int64_t)b * (K + 1) + j) * V;
+    const float invSt = (float)(1.0 / ts.S);
+    const bool dprobs = p.draft_kind == 1;
+    const int dr = draft_slot(p, b, j);
+    RowStat ds = ts;
+    float invSd = 0.f;
+    if (!dprobs) {
+        ds = load_rowstat(p.rstat + dr);
+        invSd = (float)(1.0 / ds.S);
+    }
+    const int64_t doff = ((int64_t)b * K + j) * V;
+    // p_t(v) of a target row not kept as a list
+    auto pt_at = [&](int v) -> float {
+        const float l = Elem<T>::load(trow, v);
+        return kept_prefix(ts, key_of(l), v) ? ex2_fast((l - ts.M) * c) * invSt : 0.f;
+    };
+    auto pd_at = [&](int v) -> float {
+        if (dprobs) return __ldg((const float*)p.draft + doff + v);
+        if (ds.mode == MODE_LIST) {
+            const int32_t* ids = p.kept_id + (int64_t)dr * KCAP;
+            const int i = lower_bound_i32(ids, ds.n_kept, v);
+            return (i < ds.n_kept && __ldcg(ids + i) == v)
+                       ? ex2_fast((__ldcg(p.kept_l + (int64_t)dr * KCAP + i) - ds.M) * c) * invSd
+                       : 0.f;
+        }
+        const float l = Elem<T>::load((const T*)p.draft + doff, v);
+        return kept_prefix(ds, key_of(l), v) ? ex2_fast((l - ds.M) * c) * invSd : 0.f;
+    };
+    unsigned long long part = 0;
+    if (ts.mode == MODE_LIST) {
+        const int32_t* ids = p.kept_id + (int64_t)tr * KCAP;
+        const float* ls = p.kept_l + (int64_t)tr * KCAP;
+        for (int i = threadIdx.x; i < ts.n_kept; i += NT) {
+            const float pt = ex2_fast((__ldcg(ls + i) - ts.M) * c) * invSt;
+            part += to_fix56(fminf(pt, pd_at(__ldcg(ids + i))));
+        }
+    } else if (!dprobs && ds.mode == MODE_LIST) {
+        const int32_t* ids = p.kept_id + (int64_t)dr * KCAP;
+        const float* ls = p.kept_l + (int64_t)dr * KCAP;
+        for (int i = threadIdx.x; i < ds.n_kept; i += NT) {
+            const float pd = ex2_fast((__ldcg(ls + i) - ds.M) * c) * invSd;
+            part += to_fix56(fminf(pt_at(__ldcg(ids + i)), pd));
+        }
+    } else {
+        for (int v = threadIdx.x; v < V; v += NT) part += to_fix56(fminf(pt_at(v), pd_at(v)));
+    }
+    unsigned long long total;
+    block_excl_scan<unsigned long long>(part, s_red, &total);
+    if (threadIdx.x == 0) *dst = (float)from_fix56(total);
+}
+
+cudaError_t launch_alpha(const Params& p, int dtype, cudaStream_t s)
+{
+    const int64_t slots = (int64_t)p.B * p.Kmax;
+    if (slots <= 0 || !p.alpha) return cudaSuccess;
+    if (dtype == 1) k_alpha<__nv_bfloat16><<<(unsigned)slots, NT, 0, s>>>(p);
+    else k_alpha<float><<<(unsigned)slots, NT, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s)
 {
     if (njobs <= 0 || p.nseg_sample <= 0) return cudaSuccess;

@@ -53,7 +53,7 @@ def run_gpu(w, toks, *, verifier=None, seed=None, round=None, repeat=1):
     for _ in range(repeat):
         out = verifier.run(target, draft, xt, kpr, temperature=w.temperature, top_k=w.top_k,
                            top_p=w.top_p, seed=w.seed if seed is None else seed,
-                           round=w.round if round is None else round)
+                           round=w.round if round is None else round, alpha=True)
         torch.cuda.synchronize()
         outs.append({k: v.cpu().numpy() for k, v in out.items()})
     if own:
@@ -110,4 +110,10 @@ def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL):
                 np.testing.assert_allclose(g["residual_mass"][b], o["residual_mass"][b],
                                            rtol=prob_rtol, atol=1e-7,
                                            err_msg=f"residual mass sequence {b}")
+            if "alpha" in g:
+                # alpha_j = sum_v min(p_t, p_d): each term in fp32, summed exactly
+                sure = (o["topp_margin_t"][b, :kb] >= delta) & (o["topp_margin_d"][b, :kb] >= delta)
+                np.testing.assert_allclose(g["alpha"][b, :kb][sure], o["alpha"][b, :kb][sure],
+                                           rtol=prob_rtol, atol=1e-7, err_msg=f"alpha sequence {b}")
+                assert np.all(np.isnan(g["alpha"][b, kb:]))
     return n_near
