@@ -31,6 +31,7 @@ struct spec_verify {
     unsigned* seq_ticket;
     Job* jobs;
     unsigned long long* job_seg;
+    unsigned long long* job_part;
     unsigned* job_ticket;
     unsigned long long* grab;
     unsigned* done;
@@ -101,6 +102,7 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.seq_ticket = h->seq_ticket;
     p.jobs = h->jobs;
     p.job_seg = h->job_seg;
+    p.job_part = h->job_part;
     p.job_ticket = h->job_ticket;
     p.nseg_sample = h->nseg_sample;
     p.chunk_stride = h->chunk_stride;
@@ -142,6 +144,7 @@ size_t layout_workspace(spec_verify* h, void* base)
     const size_t o_st = take(sizeof(unsigned) * cfg->max_batch);
     const size_t o_jobs = take(sizeof(Job) * h->jobs_cap);
     const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
+    const size_t o_jpart = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample * SAMPLE_PARTS);
     const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
     const size_t o_grab = take(sizeof(unsigned long long));
     const size_t o_done = take(sizeof(unsigned));
@@ -162,6 +165,7 @@ size_t layout_workspace(spec_verify* h, void* base)
         h->seq_ticket = (unsigned*)(b + o_st);
         h->jobs = (Job*)(b + o_jobs);
         h->job_seg = (unsigned long long*)(b + o_jseg);
+        h->job_part = (unsigned long long*)(b + o_jpart);
         h->job_ticket = (unsigned*)(b + o_jt);
         h->grab = (unsigned long long*)(b + o_grab);
         h->done = (unsigned*)(b + o_done);

@@ -32,6 +32,7 @@ constexpr int DIGIT_BITS = 11;      // radix digit of the general selection
 constexpr int NBINS = 1 << DIGIT_BITS;
 constexpr int SAMPLE_SEG = 4096;    // elements of one stage-2 segment
 constexpr int SAMPLE_EPT = SAMPLE_SEG / NT;
+constexpr int SAMPLE_PARTS = 4;      // per segment: partial masses of its rounds of 16-byte words
 constexpr int WALK_EPT = 16;        // contiguous elements per thread in ordered walks
 constexpr int SCRATCH_BYTES = 40960;  // shared scratch of a row merge / sequence decision
 constexpr int NSTAGE = 4;           // ring stages of the streaming kernel
@@ -120,6 +121,7 @@ struct Params {
     unsigned* seq_ticket;     // [B]
     Job* jobs;                // [njobs]
     unsigned long long* job_seg;  // [njobs, nseg_sample] fixed-point segment masses
+    unsigned long long* job_part; // [njobs, nseg_sample, SAMPLE_PARTS] the segments' round masses
     unsigned* job_ticket;     // [njobs]
     int32_t nseg_sample;      // stage-2 segments per row
     unsigned long long* grab; // streaming kernel: next work item (reset by the last CTA)
@@ -219,9 +221,24 @@ __device__ __forceinline__ float u24(uint32_t w) { return (float)(w >> 8) * 0x1p
 // Probability masses of the inverse CDF are summed as integers in units of
 // 2^-56 (a row's masses sum to at most 1, so no sum overflows), which makes
 // every partial sum exact and every scan order give the same CDF.
+// r * 2^56 rounded to nearest (ties to even) for r >= 0, from r's bits with
+// integer operations only (a float-to-u64 conversion runs on the fp64 pipe,
+// which is slow on this part); negatives and NaN give 0, values >= 2^8
+// saturate
 __device__ __forceinline__ unsigned long long to_fix56(float r)
 {
-    return __float2ull_rn(r * 0x1p56f);
+    const uint32_t u = __float_as_uint(r);
+    if (u >> 31) return 0ull;                       // negative (or -0, -NaN)
+    const int ex = (int)(u >> 23);                  // biased exponent
+    if (ex == 0) return 0ull;                       // zero or subnormal: below 2^-70
+    if (ex == 255) return (u & 0x7FFFFFu) ? 0ull : ~0ull;  // NaN, +inf
+    const unsigned long long m = (u & 0x7FFFFFu) | 0x800000u;  // r = m 2^(ex - 150)
+    const int sh = ex - 94;                         // r 2^56 = m 2^sh
+    if (sh >= 0) return sh > 39 ? ~0ull : m << sh;
+    if (sh < -24) return 0ull;                      // below 1/2
+    const int d = -sh;
+    const unsigned long long q = m >> d, rem = m & ((1ull << d) - 1ull), half = 1ull << (d - 1);
+    return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
 }
 __device__ __forceinline__ double from_fix56(unsigned long long z) { return (double)z * 0x1p-56; }
 

@@ -192,19 +192,44 @@ __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int se
             }
         }
     } else {
+        // one read of the thread's words; each warp's (max, sum exp) in fp32
+        // over its own max, the warps' pairs rescaled to the segment max and
+        // added in fp64 by the first thread
+        const unsigned FULL = 0xffffffffu;
+        uint4 w[G::ROUNDS];
         float m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < G::ROUNDS; ++i) m = fmax_nan(m, Vec16<T>::vmax(fetch(i)));
-        m = group_max_nan<NTH>(m, redf, lt, sync);
+        for (int i = 0; i < G::ROUNDS; ++i) {
+            w[i] = fetch(i);
+            m = fmax_nan(m, Vec16<T>::vmax(w[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(FULL, m, o));
         float s = 0.f;
         if (m > -INFINITY && m < INFINITY) {
 #pragma unroll
-            for (int i = 0; i < G::ROUNDS; ++i) s += Vec16<T>::vsumexp(fetch(i), m, p.c);
+            for (int i = 0; i < G::ROUNDS; ++i) s += Vec16<T>::vsumexp(w[i], m, p.c);
         }
-        const double tot = group_sum_d<NTH>((double)s, redd, lt, sync);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+        sync();  // the previous segment's pairs are read
+        if ((lt & 31) == 0) {
+            redf[lt >> 5] = m;
+            redd[lt >> 5] = (double)s;
+        }
+        sync();
         if (lt == 0) {
+            float M = redf[0];
+#pragma unroll
+            for (int i = 1; i < NTH / 32; ++i) M = fmax_nan(M, redf[i]);
+            double tot = 0.0;
+            if (M > -INFINITY && M < INFINITY) {
+#pragma unroll
+                for (int i = 0; i < NTH / 32; ++i)
+                    if (redf[i] > -INFINITY) tot += redd[i] * (double)exp2f((redf[i] - M) * p.c);
+            }
             SegStat st;
-            st.m = m;
+            st.m = M;
             st.pad = 0.f;
             st.s = tot;
             p.seg[(int64_t)r * p.nseg + seg] = st;
@@ -873,8 +898,8 @@ __device__ int sample_list(const Params& p, int tr, const RowStat& ts, bool resi
         }
         csync();
     }
-    const float invSt = (float)(1.0 / ts.S);
-    const float invSd = (residual && d.kind == 0) ? (float)(1.0 / d.st.S) : 0.f;
+    const float invSt = 1.f / (float)ts.S;
+    const float invSd = (residual && d.kind == 0) ? 1.f / (float)d.st.S : 0.f;
     const int ept = (n + NT - 1) / NT;
     const int i0 = threadIdx.x * ept;
     *zero = false;

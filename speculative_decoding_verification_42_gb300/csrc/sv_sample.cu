@@ -24,27 +24,87 @@ struct DenseJob {
     float invSd;
     const int32_t* dids;   // draft kept list (MODE_LIST)
     const float* dls;
+    bool tvec, dvec;       // rows on 16 bytes: whole words are loaded at once
 };
 
-template <typename T>
-__device__ __forceinline__ float dense_pt(const DenseJob& J, float c, int v)
+// p_t(v) from the target logit l at v
+__device__ __forceinline__ float dense_pt(const DenseJob& J, float c, float l, int v)
 {
-    const float l = Elem<T>::load((const T*)J.trow, v);
-    if (!kept_prefix(J.ts, key_of(l), v)) return 0.f;
+    if (J.ts.mode != MODE_ALL && !kept_prefix(J.ts, key_of(l), v)) return 0.f;
     return ex2_fast((l - J.ts.M) * c) * J.invSt;
 }
 
-// R(v) of the element range [v0, v1) of one thread, in fixed point; the draft
-// list (if any) is walked with a pointer
+// A thread's elements of the segment at base come in SQ 16-byte words of
+// the target row: element e of word q is base + (q NT + threadIdx.x) SW + e
+// (consecutive threads read consecutive words).  All of them are loaded
+// before any is used, so the loads share one round trip.
+template <typename T> struct SampleGeom {
+    static constexpr int SW = 16 / (int)sizeof(T);  // elements per word
+    static constexpr int SQ = SAMPLE_EPT / SW;       // words per thread
+};
+static_assert(SampleGeom<float>::SQ <= SAMPLE_PARTS && SampleGeom<__nv_bfloat16>::SQ <= SAMPLE_PARTS,
+              "a segment's rounds fit its partial masses");
+
 template <typename T>
-__device__ __forceinline__ unsigned long long dense_r_fix(const DenseJob& J, float c, int v,
+__device__ __forceinline__ int word_at(int base, int q, int t = (int)threadIdx.x)
+{
+    return base + (q * NT + t) * SampleGeom<T>::SW;
+}
+
+// SW elements of a row of U at v0 (16-byte aligned when vec) into out
+template <typename U, int SW>
+__device__ __forceinline__ void load_word(const U* row, int v0, int V, bool vec, float fill, float* out)
+{
+    if (vec && v0 + SW <= V) {
+        constexpr int NV = SW * (int)sizeof(U) / 16;  // 16-byte loads
+#pragma unroll
+        for (int g = 0; g < NV; ++g) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + v0) + g);
+            const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+            if (sizeof(U) == 4) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) out[g * 4 + i] = __uint_as_float(x[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    out[g * 8 + 2 * i] = bf16_lo(x[i]);
+                    out[g * 8 + 2 * i + 1] = bf16_hi(x[i]);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < SW; ++e) out[e] = v0 + e < V ? Elem<U>::load(row, v0 + e) : fill;
+    }
+}
+
+// the target logits and (when read densely) draft values of the word at v0
+template <typename T>
+__device__ __forceinline__ void load_word_vals(const DenseJob& J, int v0, int V, float* lt, float* dv)
+{
+    constexpr int SW = SampleGeom<T>::SW;
+    load_word<T, SW>((const T*)J.trow, v0, V, J.tvec, -INFINITY, lt);
+    if (!J.residual || (J.dkind == 0 && J.ds.mode == MODE_LIST)) {
+#pragma unroll
+        for (int e = 0; e < SW; ++e) dv[e] = 0.f;
+    } else if (J.dkind == 1) {
+        load_word<float, SW>((const float*)J.drow, v0, V, J.dvec, 0.f, dv);
+    } else {
+        load_word<T, SW>((const T*)J.drow, v0, V, J.dvec, -INFINITY, dv);
+    }
+}
+
+// R(v) in fixed point from the target logit l and draft value d at v (v
+// ascending over the calls of one walk); the draft list (if any) is walked
+// with a pointer
+__device__ __forceinline__ unsigned long long dense_r_fix(const DenseJob& J, float c, float l, float d, int v,
                                                           int& dptr)
 {
-    const float pt = dense_pt<T>(J, c, v);
+    const float pt = dense_pt(J, c, l, v);
     if (!J.residual) return to_fix56(pt);
     float pd;
     if (J.dkind == 1) {
-        pd = __ldg((const float*)J.drow + v);
+        pd = d;
     } else if (J.ds.mode == MODE_LIST) {
         const int n = J.ds.n_kept;
         while (dptr < n && __ldcg(J.dids + dptr) < v) ++dptr;
@@ -52,22 +112,32 @@ __device__ __forceinline__ unsigned long long dense_r_fix(const DenseJob& J, flo
                  ? ex2_fast((__ldcg(J.dls + dptr) - J.ds.M) * c) * J.invSd
                  : 0.f;
     } else {
-        const float l = Elem<T>::load((const T*)J.drow, v);
-        pd = kept_prefix(J.ds, key_of(l), v) ? ex2_fast((l - J.ds.M) * c) * J.invSd : 0.f;
+        pd = kept_prefix(J.ds, key_of(d), v) ? ex2_fast((d - J.ds.M) * c) * J.invSd : 0.f;
     }
     return to_fix56(fmaxf(pt - pd, 0.f));
 }
 
+// the fixed-point mass of each of the thread's words of the segment at base
+// (all loads first)
 template <typename T>
-__device__ __forceinline__ unsigned long long thread_part(const DenseJob& J, float c, int v0,
-                                                          int v1)
+__device__ __forceinline__ void word_masses(const DenseJob& J, float c, int base, int V,
+                                            unsigned long long (&wm)[SampleGeom<T>::SQ])
 {
+    using G = SampleGeom<T>;
+    float lt[SAMPLE_EPT], dv[SAMPLE_EPT];
+#pragma unroll
+    for (int q = 0; q < G::SQ; ++q) load_word_vals<T>(J, word_at<T>(base, q), V, lt + q * G::SW, dv + q * G::SW);
     int dptr = 0;
-    if (J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST && v0 < v1)
-        dptr = lower_bound_i32(J.dids, J.ds.n_kept, v0);
-    unsigned long long part = 0;
-    for (int v = v0; v < v1; ++v) part += dense_r_fix<T>(J, c, v, dptr);
-    return part;
+    if (J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST)
+        dptr = lower_bound_i32(J.dids, J.ds.n_kept, min(word_at<T>(base, 0), V));
+#pragma unroll
+    for (int q = 0; q < G::SQ; ++q) {
+        const int v0 = word_at<T>(base, q);
+        wm[q] = 0ull;
+#pragma unroll
+        for (int e = 0; e < G::SW; ++e)
+            if (v0 + e < V) wm[q] += dense_r_fix(J, c, lt[q * G::SW + e], dv[q * G::SW + e], v0 + e, dptr);
+    }
 }
 
 template <typename T>
@@ -78,7 +148,7 @@ __device__ DenseJob make_job(const Params& p, const Job& jb, bool residual)
     const int rps = p.rps;
     const int64_t V = p.V;
     J.ts = load_rowstat(p.rstat + jb.trow);
-    J.invSt = (float)(1.0 / J.ts.S);
+    J.invSt = 1.f / (float)J.ts.S;
     {
         const int b = jb.trow / rps, slot = jb.trow - b * rps;
         const bool is_draft = p.draft_launch || slot > p.Kmax;
@@ -86,6 +156,7 @@ __device__ DenseJob make_job(const Params& p, const Job& jb, bool residual)
         const int64_t off = is_draft ? ((int64_t)b * p.Kmax + j) * V : ((int64_t)b * (p.Kmax + 1) + j) * V;
         J.trow = (const T*)(is_draft ? p.draft : p.target) + off;
     }
+    J.tvec = ((uintptr_t)J.trow & 15u) == 0;
     J.dkind = p.draft_kind;
     J.drow = nullptr;
     J.dids = nullptr;
@@ -100,37 +171,56 @@ __device__ DenseJob make_job(const Params& p, const Job& jb, bool residual)
         } else {
             J.drow = (const T*)p.draft + off;
             J.ds = load_rowstat(p.rstat + jb.drow);
-            J.invSd = (float)(1.0 / J.ds.S);
+            J.invSd = 1.f / (float)J.ds.S;
             J.dids = p.kept_id + (int64_t)jb.drow * KCAP;
             J.dls = p.kept_l + (int64_t)jb.drow * KCAP;
         }
     }
+    J.dvec = J.drow && ((uintptr_t)J.drow & 15u) == 0;
     return J;
 }
 
-// fixed-point mass of one segment (block total); every thread gets it
+// one segment's pass: the fixed-point masses summed per round q (NT
+// consecutive words) into parts[q] (smem s_part, then global), the segment
+// total returned to thread 0 (integer sums: the order of the terms is free)
 template <typename T>
-__device__ unsigned long long segment_mass(const DenseJob& J, float c, int V, int seg,
-                                           unsigned long long* red, unsigned long long* ex_out,
-                                           unsigned long long* part_out, int* v0_out, int* v1_out)
+__device__ unsigned long long segment_pass(const DenseJob& J, float c, int V, int seg,
+                                           unsigned long long* parts, unsigned long long* s_part,
+                                           unsigned long long* s_red)
 {
-    const int base = seg * SAMPLE_SEG;
-    const int v0 = min(V, base + (int)threadIdx.x * SAMPLE_EPT);
-    const int v1 = min(V, v0 + SAMPLE_EPT);
-    const unsigned long long part = thread_part<T>(J, c, v0, v1);
-    unsigned long long total;
-    const unsigned long long ex = block_excl_scan<unsigned long long>(part, red, &total);
-    if (ex_out) *ex_out = ex;
-    if (part_out) *part_out = part;
-    if (v0_out) *v0_out = v0;
-    if (v1_out) *v1_out = v1;
+    using G = SampleGeom<T>;
+    unsigned long long wm[G::SQ];
+    word_masses<T>(J, c, seg * SAMPLE_SEG, V, wm);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int q = 0; q < G::SQ; ++q) {
+        unsigned long long w = wm[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (lane == 0) s_part[q * (NT / 32) + warp] = w;
+    }
+    __syncthreads();
+    unsigned long long total = 0;
+    if (threadIdx.x < G::SQ) {
+        unsigned long long r = 0;
+        for (int i = 0; i < NT / 32; ++i) r += s_part[threadIdx.x * (NT / 32) + i];
+        parts[threadIdx.x] = r;
+        s_red[threadIdx.x] = r;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int q = 0; q < G::SQ; ++q) total += s_red[q];
+    __syncthreads();  // s_part and s_red may be reused
     return total;
 }
 
 template <typename T>
-__global__ void __launch_bounds__(NT) k_sample(const Params p)
+__global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
 {
+    using G = SampleGeom<T>;
     __shared__ unsigned long long s_red[NT / 32 + 1];
+    __shared__ unsigned long long s_part[4 * (NT / 32)];
+    __shared__ unsigned long long s_base;
     __shared__ int s_last, s_star, s_tok;
     const int V = p.V, nseg = p.nseg_sample;
     const int jid = blockIdx.x / nseg, seg = blockIdx.x - jid * nseg;
@@ -138,21 +228,23 @@ __global__ void __launch_bounds__(NT) k_sample(const Params p)
     if (jb.kind == JOB_NONE) return;
     const bool residual = jb.kind == JOB_RESIDUAL;
     DenseJob J = make_job<T>(p, jb, residual);
+    unsigned long long* parts = p.job_part + (int64_t)jid * nseg * SAMPLE_PARTS;
 
     const unsigned long long zs =
-        segment_mass<T>(J, p.c, V, seg, s_red, nullptr, nullptr, nullptr, nullptr);
-    if (threadIdx.x == 0) p.job_seg[(int64_t)jid * nseg + seg] = zs;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&p.job_ticket[jid], 1u) == (unsigned)(nseg - 1);
+        segment_pass<T>(J, p.c, V, seg, parts + (int64_t)seg * SAMPLE_PARTS, s_part, s_red);
+    if (threadIdx.x == 0) {
+        p.job_seg[(int64_t)jid * nseg + seg] = zs;
+        __threadfence();  // the segment's masses are visible before its ticket
+        s_last = atomicAdd(&p.job_ticket[jid], 1u) == (unsigned)(nseg - 1);
+        if (s_last) __threadfence();
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
+    // ---- the last segment of the job: locate u Z, segment -> part -> element
     if (threadIdx.x == 0) {
         p.job_ticket[jid] = 0u;
         s_tok = -1;
     }
-
     unsigned long long* seg_tot = p.job_seg + (int64_t)jid * nseg;
     bool zero = false;
     unsigned long long Z0 = 0;
@@ -161,13 +253,13 @@ __global__ void __launch_bounds__(NT) k_sample(const Params p)
             // the residual summed to 0 (rounding only): sample p_t itself
             zero = true;
             J.residual = false;
-            for (int s = 0; s < nseg; ++s) {
+            for (int sg = 0; sg < nseg; ++sg) {
                 const unsigned long long z =
-                    segment_mass<T>(J, p.c, V, s, s_red, nullptr, nullptr, nullptr, nullptr);
-                if (threadIdx.x == 0) seg_tot[s] = z;
-                __syncthreads();
+                    segment_pass<T>(J, p.c, V, sg, parts + (int64_t)sg * SAMPLE_PARTS, s_part, s_red);
+                if (threadIdx.x == 0) seg_tot[sg] = z;
             }
             __threadfence_block();
+            __syncthreads();
         }
         const unsigned long long z = threadIdx.x < nseg ? __ldcg(seg_tot + threadIdx.x) : 0ull;
         unsigned long long Z;
@@ -178,32 +270,53 @@ __global__ void __launch_bounds__(NT) k_sample(const Params p)
             break;  // nothing to sample (cannot happen for a finite row)
         }
         const unsigned long long t = cdf_target(jb.u, Z);
-        if (threadIdx.x == 0) {
-            s_star = -1;
-            s_tok = -1;
-        }
+        if (threadIdx.x == 0) s_star = -1;
         __syncthreads();
-        if (threadIdx.x < nseg && exs <= t && t < exs + z) s_star = threadIdx.x;
+        if (threadIdx.x < nseg && exs <= t && t < exs + z) {
+            s_star = threadIdx.x;
+            s_base = exs;
+        }
         __syncthreads();
         const int star = s_star;
         if (star < 0) break;  // no segment holds u Z (cannot happen when Z > 0)
-        __shared__ unsigned long long s_base;
-        if (threadIdx.x == star) s_base = exs;
+        // the round of the crossing segment holding u Z (thread 0, in order)
+        if (threadIdx.x == 0) {
+            unsigned long long acc = s_base;
+            s_star = G::SQ - 1;
+            for (int q = 0; q < G::SQ; ++q) {
+                const unsigned long long rq = __ldcg(parts + (int64_t)star * SAMPLE_PARTS + q);
+                if (t < acc + rq) {
+                    s_star = q;
+                    break;
+                }
+                acc += rq;
+            }
+            s_base = acc;  // the mass before that round
+        }
         __syncthreads();
-        // rescan the crossing segment: same per-thread partials, same order
-        unsigned long long ex, part;
-        int v0, v1;
-        segment_mass<T>(J, p.c, V, star, s_red, &ex, &part, &v0, &v1);
-        const unsigned long long before = s_base + ex;
-        if (before <= t && t < before + part) {
-            int dptr = 0;
-            if (J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST)
-                dptr = lower_bound_i32(J.dids, J.ds.n_kept, v0);
-            unsigned long long acc = before;
-            for (int v = v0; v < v1; ++v) {
-                acc += dense_r_fix<T>(J, p.c, v, dptr);
+        const int qs = s_star;
+        // that round again, one word per thread, then the thread and element
+        const int v0 = word_at<T>(star * SAMPLE_SEG, qs);
+        float lt[G::SW], dv[G::SW];
+        load_word_vals<T>(J, v0, V, lt, dv);
+        int dptr = 0;
+        if (J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST)
+            dptr = lower_bound_i32(J.dids, J.ds.n_kept, min(v0, V));
+        unsigned long long em[G::SW], mine = 0;
+#pragma unroll
+        for (int e = 0; e < G::SW; ++e) {
+            em[e] = v0 + e < V ? dense_r_fix(J, p.c, lt[e], dv[e], v0 + e, dptr) : 0ull;
+            mine += em[e];
+        }
+        unsigned long long rtot;
+        const unsigned long long ex = block_excl_scan<unsigned long long>(mine, s_red, &rtot);
+        unsigned long long acc = s_base + ex;
+        if (mine > 0ull && acc <= t && t < acc + mine) {
+#pragma unroll
+            for (int e = 0; e < G::SW; ++e) {
+                acc += em[e];
                 if (acc > t) {
-                    s_tok = v;
+                    s_tok = v0 + e;
                     break;
                 }
             }
@@ -233,7 +346,7 @@ __global__ void __launch_bounds__(NT) k_probs(const Params p)
     const int64_t off = row_elem_offset(p, rr);
     const T* row = (const T*)p.draft + off;
     float* out = p.probs_out + off;
-    const float invS = (float)(1.0 / st.S);
+    const float invS = 1.f / (float)st.S;
     const int32_t* ids = p.kept_id + (int64_t)r * KCAP;
     const float* ls = p.kept_l + (int64_t)r * KCAP;
     for (int v = threadIdx.x; v < p.V; v += NT) {
@@ -276,14 +389,14 @@ __global__ void __launch_bounds__(NT) k_alpha(const Params p)
     const int tr = target_slot(p, b, j);
     const RowStat ts = load_rowstat(p.rstat + tr);
     const T* trow = (const T*)p.target + ((int64_t)b * (K + 1) + j) * V;
-    const float invSt = (float)(1.0 / ts.S);
+    const float invSt = 1.f / (float)ts.S;
     const bool dprobs = p.draft_kind == 1;
     const int dr = draft_slot(p, b, j);
     RowStat ds = ts;
     float invSd = 0.f;
     if (!dprobs) {
         ds = load_rowstat(p.rstat + dr);
-        invSd = (float)(1.0 / ds.S);
+        invSd = 1.f / (float)ds.S;
     }
     const int64_t doff = ((int64_t)b * K + j) * V;
     // p_t(v) of a target row not kept as a list

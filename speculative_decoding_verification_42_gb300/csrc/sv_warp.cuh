@@ -315,7 +315,7 @@ __device__ __forceinline__ void warp_all_stats(const Params& p, int r, RowStat& 
     for (int i = lane; i < p.nseg; i += 32) {
         const SegStat* g = p.seg + (int64_t)r * p.nseg + i;
         const float gm = __ldcg(&g->m);
-        if (gm > -INFINITY) s += __ldcg(&g->s) * exp2(((double)gm - (double)m) * (double)p.c);
+        if (gm > -INFINITY) s += __ldcg(&g->s) * (double)exp2f((gm - m) * p.c);
     }
     st.M = m;
     st.S = warp_sum_d(s);
