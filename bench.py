@@ -526,6 +526,17 @@ def run_gpu(args):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clocks,
     }
+    if fused:
+        # the verify stage of the fused round: the step without the LM head,
+        # against the bytes of its rows (target logits + draft probabilities)
+        vb = w.logit_bytes()
+        v_us = (mean_step_ms - mean_kern_ms) * 1e3
+        line["verify_stage"] = {"us": v_us, "algorithmic_bytes": vb,
+                                "achieved_gbs": vb / (v_us * 1e-6) / 1e9,
+                                "frac": vb / (v_us * 1e-6) / 1e9 / peak,
+                                "note": "step time minus the LM head's live time; the kernels "
+                                        "read the draft probabilities only at drafted tokens "
+                                        "and at the resampled row"}
     if flops:
         tf = _tensor_peak()
         line["roofline"]["tensor"] = {

@@ -127,6 +127,9 @@ size_t layout_workspace(spec_verify* h, void* base)
         h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, seg_elems(dt)));
         h->nchunk_cap = (int)std::max<int64_t>(h->nchunk_cap, cdiv(V, chunk_elems(dt)));
     }
+    // the LM head's softmax partials: one per 256-column tile
+    if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD)
+        h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, LM_STAT_COLS));
     h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
     h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
     size_t off = 0;
@@ -342,16 +345,30 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
     int launches = 0;
+    // rows without top-k / top-p after the LM head: its epilogue writes the
+    // softmax partials per 256-column tile and no stream pass is needed
+    const bool lm_stats = lmhead && p.seg_mode == SEG_SUM && warp_merge_ok(p);
     if (lmhead) {
         // the hook times the LM head, the kernel that reads W_vocab
         if (h->prof_begin && cudaEventRecord(h->prof_begin, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        LmStats st{nullptr, 0, 1, 1, 0.f};
+        if (lm_stats) {
+            p.nseg = (int)cdiv(p.V, LM_STAT_COLS);
+            st = LmStats{h->seg, p.nseg, in->k_max + 1, p.rps, p.c};
+        }
         if (launch_lmhead(in->target, in->w_vocab, h->logits, m_rows, cfg.vocab, cfg.hidden, cfg.vocab,
-                          h->err, cs) != cudaSuccess)
+                          h->err, cs, st) != cudaSuccess)
             return SPEC_ERR_CUDA;
         if (h->prof_end && cudaEventRecord(h->prof_end, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;
     }
-    if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (lm_stats) {
+        // the row merge (softmax partials of the LM head) and the decision grid
+        launches += 2;
+        if (launch_merge_warp(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead) != cudaSuccess) {
+        return SPEC_ERR_CUDA;
+    }
     if (!all_lists(p)) {
         if (launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;

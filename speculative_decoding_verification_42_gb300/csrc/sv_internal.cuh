@@ -569,8 +569,17 @@ cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s)
 cudaError_t launch_alpha(const Params& p, int dtype, cudaStream_t s);
 // the LM head: out[M, N] (row stride ldo) = hidden[M, K] x w[K, N], bf16 in, fp32 out
 bool lmhead_shape_ok(const void* hidden, const void* w, int M, int N, int K);
+// softmax partials the LM head's epilogue writes (seg NULL: none): per
+// logits row m = b kp1 + j and 256-column tile n, (max, sum exp2((l - max)
+// c)) at seg[(b rps + j) nseg + n]
+constexpr int LM_STAT_COLS = 256;
+struct LmStats {
+    SegStat* seg;
+    int nseg, kp1, rps;
+    float c;
+};
 cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, int N, int K, int64_t ldo,
-                          unsigned* err, cudaStream_t s);
+                          unsigned* err, cudaStream_t s, const LmStats& st = LmStats{nullptr, 0, 1, 1, 0.f});
 cudaError_t launch_probs(const Params& p, int dtype, cudaStream_t s);
 
 }  // namespace sv

@@ -17,7 +17,10 @@
 // with a multicast tcgen05.commit; warps 2..5 read the other accumulator back
 // (tcgen05.ld, one row per thread) and store the fp32 tile meanwhile.  H is
 // the K-major A operand; W, whose rows run along the vocabulary, is the
-// N-major B operand.
+// N-major B operand.  On request the epilogue also writes, per row and
+// 256-column tile, the softmax partials (max, sum exp2((l - max) c)) that
+// the verify's row merge combines, so that no pass over the logits is needed
+// for rows without top-k / top-p.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
 
 #include <algorithm>
@@ -37,6 +40,7 @@ constexpr int LM_THREADS = 192;                     // producer, MMA, four epilo
 constexpr uint32_t LM_ACC_COLS = 256;               // fp32 accumulator: 128 lanes x 256 columns
 constexpr uint32_t LM_TMEM_COLS = 2 * LM_ACC_COLS;  // two accumulators
 static_assert(LM_BN == 4 * 64, "each CTA of the pair copies two 64-column boxes of W");
+static_assert(LM_BN == LM_STAT_COLS, "the softmax partials are per column tile");
 
 // ------------------------------------------------------------------------- //
 // PTX wrappers                                                              //
@@ -140,7 +144,7 @@ __device__ __forceinline__ void lm_ld32(uint32_t taddr, uint32_t (&v)[32])
 // ------------------------------------------------------------------------- //
 __global__ void __launch_bounds__(LM_THREADS, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
-             float* __restrict__ out, int M, int N, int K, int64_t ldo, unsigned* err)
+             float* __restrict__ out, int M, int N, int K, int64_t ldo, unsigned* err, LmStats st)
 {
     extern __shared__ unsigned char lm_smem_raw[];
     __shared__ __align__(8) uint64_t full[LM_STAGES];   // stage loaded (own H + both W halves)
@@ -259,10 +263,27 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
             const int n0 = (t / n_mpair) * LM_BN;
             const int row = m0 + q * 32 + lane;
             const uint32_t src = tmem + acc * LM_ACC_COLS + ((uint32_t)(q * 32) << 16);
+            float tmx = -INFINITY, tsum = 0.f;  // the row's (max, sum exp2((l - max) c)) over the tile
 #pragma unroll 1
             for (int c = 0; c < LM_BN; c += 32) {
                 uint32_t v[32];
                 lm_ld32(src + (uint32_t)c, v);
+                if (st.seg) {
+                    const int nvalid = min(32, N - (n0 + c));
+                    float cm = -INFINITY;
+#pragma unroll
+                    for (int g = 0; g < 32; ++g)
+                        if (g < nvalid) cm = fmax_nan(cm, __uint_as_float(v[g]));
+                    const float nm = fmax_nan(tmx, cm);
+                    if (nm > -INFINITY && nm < INFINITY) {
+                        float add = 0.f;
+#pragma unroll
+                        for (int g = 0; g < 32; ++g)
+                            if (g < nvalid) add += ex2_fast((__uint_as_float(v[g]) - nm) * st.c);
+                        tsum = tsum * ex2_fast((tmx - nm) * st.c) + add;
+                    }
+                    tmx = nm;
+                }
                 if (row < M) {
                     float* o = out + (int64_t)row * ldo + n0 + c;
                     const int nvalid = min(32, N - (n0 + c));
@@ -278,6 +299,15 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                             if (g < nvalid) o[g] = __uint_as_float(v[g]);
                     }
                 }
+            }
+            if (st.seg && row < M && n0 < N) {
+                // the verify's row slot of logits row `row` (position j of sequence b)
+                const int b = row / st.kp1, j = row - b * st.kp1;
+                SegStat ss;
+                ss.m = tmx;
+                ss.pad = 0.f;
+                ss.s = (double)tsum;
+                st.seg[((int64_t)b * st.rps + j) * st.nseg + n0 / LM_BN] = ss;
             }
             tc_fence_before();
             __syncwarp();
@@ -340,7 +370,7 @@ bool lmhead_shape_ok(const void* hidden, const void* w, int M, int N, int K)
 }
 
 cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, int N, int K, int64_t ldo,
-                          unsigned* err, cudaStream_t s)
+                          unsigned* err, cudaStream_t s, const LmStats& st)
 {
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg = {};
@@ -374,7 +404,7 @@ cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, 
     const int n_mpair = ((M + LM_BM - 1) / LM_BM + 1) / 2;
     const int n_tiles = n_mpair * ((N + LM_BN - 1) / LM_BN);
     cfg.gridDim = dim3((unsigned)(2 * std::min(n_tiles, max_clusters)));
-    return cudaLaunchKernelEx(&cfg, k_lmhead, mh, mw, out, M, N, K, ldo, err);
+    return cudaLaunchKernelEx(&cfg, k_lmhead, mh, mw, out, M, N, K, ldo, err, st);
 }
 
 }  // namespace sv
