@@ -303,19 +303,39 @@ __device__ __forceinline__ void warp_all_stats(const Params& p, int r, RowStat& 
 {
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
+    constexpr int PER = 16;  // segment records a lane holds (one round of loads)
+    const uint4* seg = reinterpret_cast<const uint4*>(p.seg + (int64_t)r * p.nseg);
     float m = -INFINITY;
-    for (int i = lane; i < p.nseg; i += 32) m = fmax_nan(m, __ldcg(&p.seg[(int64_t)r * p.nseg + i].m));
+    double s = 0.0;
+    for (int i0 = 0; i0 < p.nseg; i0 += 32 * PER) {
+        uint4 w[PER];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(FULL, m, o));
+        for (int k = 0; k < PER; ++k) {
+            const int i = i0 + k * 32 + lane;
+            w[k] = i < p.nseg ? __ldcg(seg + i) : make_uint4(0xFF800000u, 0u, 0u, 0u);  // (-inf, 0)
+        }
+        float mb = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) mb = fmax_nan(mb, __uint_as_float(w[k].x));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mb = fmax_nan(mb, __shfl_xor_sync(FULL, mb, o));
+        const float nm = fmax_nan(m, mb);
+        if (!(nm > -INFINITY && nm < INFINITY)) {
+            m = nm;
+            continue;  // no finite maximum yet (or NaN / +inf: flagged below)
+        }
+        if (m > -INFINITY) s *= (double)exp2f((m - nm) * p.c);
+        m = nm;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const float gm = __uint_as_float(w[k].x);
+            const double gs = __hiloint2double((int)w[k].w, (int)w[k].z);
+            if (gm > -INFINITY) s += gs * (double)exp2f((gm - m) * p.c);
+        }
+    }
     if (!(m > -INFINITY && m < INFINITY)) {
         st.flags = FLAG_NONFINITE;
         return;
-    }
-    double s = 0.0;
-    for (int i = lane; i < p.nseg; i += 32) {
-        const SegStat* g = p.seg + (int64_t)r * p.nseg + i;
-        const float gm = __ldcg(&g->m);
-        if (gm > -INFINITY) s += __ldcg(&g->s) * (double)exp2f((gm - m) * p.c);
     }
     st.M = m;
     st.S = warp_sum_d(s);
