@@ -165,6 +165,25 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in,
                             const spec_sampling* s, const spec_verify_outputs* out,
                             void* stream);
 
+/* The same verify with early exit (NEXT f2): for each sequence the target and
+ * draft rows of position j are read only when every draft before j was
+ * accepted, since the drafts after the first rejection are discarded
+ * ("Accelerating Large Language Model Decoding with Speculative Sampling",
+ * The algorithm), so the bytes read fall from 2 K_b + 1 rows to about
+ * 2 sum_j alpha^j.  Each CTA walks whole sequences: it pays at large B, and
+ * at small B (fewer sequences than SMs) the full verify is faster.
+ * It applies to rows of logits on 16 bytes with 1 <= top-k <= 128 (or
+ * greedy) and no LM head; otherwise it runs spec_verify_run.
+ * Results are those of spec_verify_run except that
+ *  - a NaN or +inf logit in a row after the first rejection is not seen;
+ *  - p_t / p_d at the drafted tokens and target_lse are written for the
+ *    positions read and NaN beyond; alpha is NaN.
+ * Rows whose top-k candidates overflow its staging (heavy ties) make the
+ * regular pipeline, enqueued behind it, recompute the whole batch. */
+spec_status spec_verify_run_early_exit(spec_verify_t h, const spec_verify_inputs* in,
+                                       const spec_sampling* s, const spec_verify_outputs* out,
+                                       void* stream);
+
 /* Draft-side sampler, the step before the verify: x = sample(q) of the listing
  * "One speculative decoding loop" ("57 Speculative Decoding").  For every
  * sequence b and slot j < K_b: draws draft_tokens[b, j] ~ P_d[b, j] (the draft

@@ -28,7 +28,7 @@ SPEC_ROW_OK, SPEC_ROW_BAD_TOKEN, SPEC_ROW_BAD_K, SPEC_ROW_NONFINITE, \
 # every function the header declares (checked by the tests)
 ABI_FUNCTIONS = ("spec_verify_create", "spec_verify_run", "spec_draft_sample",
                  "spec_verify_destroy", "spec_verify_status_string", "spec_verify_run_noalloc",
-                 "spec_verify_set_profiling", "spec_lmhead_logits")
+                 "spec_verify_set_profiling", "spec_lmhead_logits", "spec_verify_run_early_exit")
 SPEC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -130,6 +130,14 @@ def spec_verify_run(h, inputs: spec_verify_inputs, sampling: spec_sampling,
            "spec_verify_run")
 
 
+def spec_verify_run_early_exit(h, inputs: spec_verify_inputs, sampling: spec_sampling,
+                               outputs: spec_verify_outputs, stream: int = 0) -> None:
+    """The verify reading each sequence's rows only up to its first rejection."""
+    _check(load_library().spec_verify_run_early_exit(h, C.byref(inputs), C.byref(sampling),
+                                                     C.byref(outputs), C.c_void_p(stream)),
+           "spec_verify_run_early_exit")
+
+
 def spec_draft_sample(h, draft: int, k_per_row: int | None, batch: int, k_max: int,
                       sampling: spec_sampling, draft_tokens: int, draft_probs: int | None,
                       stream: int = 0) -> None:
@@ -228,10 +236,11 @@ class Verifier:
 
     def run(self, target, draft, draft_tokens, k_per_row=None, *, temperature=1.0, top_k=0,
             top_p=1.0, seed=0, round=0, out: dict | None = None, debug: bool = True,
-            stream=None, w_vocab=None, alpha: bool = False) -> dict:
+            stream=None, w_vocab=None, alpha: bool = False, early_exit: bool = False) -> dict:
         """Verify a batch; returns (and fills) a dict of output tensors.  With the
         LM head, ``target`` is the hidden states [B * (K + 1), H] and ``w_vocab``
-        the [H, V] matrix.  alpha: also the acceptance statistic of every slot."""
+        the [H, V] matrix.  alpha: also the acceptance statistic of every slot.
+        early_exit: read each sequence's rows only up to its first rejection."""
         import torch
         if w_vocab is not None:
             B, K = draft_tokens.shape[0], draft_tokens.shape[1]
@@ -256,8 +265,8 @@ class Verifier:
                                  _ptr(k_per_row), B, K)
         outs = spec_verify_outputs(*[_ptr(out.get(f)) for f, _ in spec_verify_outputs._fields_])
         s = stream if stream is not None else torch.cuda.current_stream(dev)
-        spec_verify_run(self.h, ins, self.sampling(temperature, top_k, top_p, seed, round), outs,
-                        s.cuda_stream)
+        run = spec_verify_run_early_exit if early_exit else spec_verify_run
+        run(self.h, ins, self.sampling(temperature, top_k, top_p, seed, round), outs, s.cuda_stream)
         return out
 
     def draft_sample(self, draft, k_per_row=None, *, temperature=1.0, top_k=0, top_p=1.0,

@@ -37,6 +37,7 @@ struct spec_verify {
     unsigned* done;
     unsigned* err;
     unsigned* seq_done;
+    unsigned* exit_flag;  // early exit: a sequence was left to the regular pipeline
     // spec_verify_set_profiling: events around the stage-1 stream kernel and
     // where each run stores the number of kernels it launched (all optional)
     cudaEvent_t prof_begin;
@@ -153,6 +154,7 @@ size_t layout_workspace(spec_verify* h, void* base)
     const size_t o_done = take(sizeof(unsigned));
     const size_t o_err = take(sizeof(unsigned));
     const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
+    const size_t o_xf = take(sizeof(unsigned));
     const bool lmhead = cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
     const size_t o_logits =
         lmhead ? take(sizeof(float) * (size_t)cfg->max_batch * (cfg->max_k + 1) * (size_t)V) : 0;
@@ -174,6 +176,7 @@ size_t layout_workspace(spec_verify* h, void* base)
         h->done = (unsigned*)(b + o_done);
         h->err = (unsigned*)(b + o_err);
         h->seq_done = (unsigned*)(b + o_sd);
+        h->exit_flag = (unsigned*)(b + o_xf);
         h->logits = lmhead ? (float*)(b + o_logits) : nullptr;
     }
     return off;
@@ -292,8 +295,9 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
     return SPEC_OK;
 }
 
-spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const spec_sampling* s,
-                            const spec_verify_outputs* out, void* stream)
+namespace {
+spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec_sampling* s,
+                       const spec_verify_outputs* out, void* stream, bool early_exit)
 {
     if (!h || !in || !s || !out) return SPEC_ERR_INVALID_ARG;
     const spec_verify_config& cfg = h->cfg;
@@ -362,11 +366,23 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
         if (h->prof_end && cudaEventRecord(h->prof_end, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;
     }
+    // early exit (top-k rows of logits): one kernel walks each sequence's
+    // positions and stops at the first rejection; the regular pipeline after
+    // it returns at once unless that kernel raised the flag
+    const bool exit = early_exit && p.cand && !lmhead;
+    if (exit) {
+        p.exit_flag = h->exit_flag;
+        if (cudaMemsetAsync(h->exit_flag, 0, sizeof(unsigned), cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (h->prof_begin && cudaEventRecord(h->prof_begin, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (launch_verify_exit(p, dtype, h->num_sms, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (h->prof_end && cudaEventRecord(h->prof_end, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+        ++launches;
+    }
     if (lm_stats) {
         // the row merge (softmax partials of the LM head) and the decision grid
         launches += 2;
         if (launch_merge_warp(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
-    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead) != cudaSuccess) {
+    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead && !exit) != cudaSuccess) {
         return SPEC_ERR_CUDA;
     }
     if (!all_lists(p)) {
@@ -379,6 +395,19 @@ spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const
     }
     if (h->prof_launches) *h->prof_launches = launches;
     return SPEC_OK;
+}
+}  // namespace
+
+spec_status spec_verify_run(spec_verify_t h, const spec_verify_inputs* in, const spec_sampling* s,
+                            const spec_verify_outputs* out, void* stream)
+{
+    return run_verify(h, in, s, out, stream, false);
+}
+
+spec_status spec_verify_run_early_exit(spec_verify_t h, const spec_verify_inputs* in, const spec_sampling* s,
+                                       const spec_verify_outputs* out, void* stream)
+{
+    return run_verify(h, in, s, out, stream, true);
 }
 
 spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t* k_per_row,

@@ -128,6 +128,7 @@ struct Params {
     unsigned* done;           // streaming kernel: CTAs finished
     unsigned* err;            // bounded waits that ran out (0 = none)
     int32_t cand;             // 1: top-k rows (1 <= top-k <= CAND_TOPK_MAX) take k_merge_cand
+    unsigned* exit_flag;      // early exit: the regular pipeline runs only when it is nonzero (NULL: always)
     unsigned* seq_done;       // [B] sequences decided inside the merge grid
 };
 
@@ -545,9 +546,19 @@ cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_
 // top-k rows: the row merge (one CTA per row) and the decision grid for what
 // it leaves, both programmatic dependents of the stream
 cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s);
+// early-exit verify of the top-k rows (one CTA per sequence at a time)
+cudaError_t launch_verify_exit(const Params& p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);
 cudaError_t launch_merge_warp(const Params& p, int dtype, cudaStream_t s);
 // rows whose merge the warp kernel handles: fast top-k rows, or rows without knobs
+// the regular pipeline after the early-exit kernel: nothing to do unless
+// that kernel left a sequence it could not finish (read after the stream's
+// previous grids have completed)
+__device__ __forceinline__ bool exit_skip(const Params& p)
+{
+    return p.exit_flag && __ldcg(p.exit_flag) == 0u;
+}
+
 // draft rows the verify streams and merges: logits, unless greedy
 __host__ __device__ __forceinline__ bool drafts_streamed(const Params& p)
 {

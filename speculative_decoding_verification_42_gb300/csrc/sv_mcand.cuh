@@ -98,10 +98,11 @@ __device__ __forceinline__ int mc_excl_scan(int v, int* red, int* total)
     return before + x - v;
 }
 
-// the merge of top-k row r by the MC_T threads; then the sequence ticket and,
-// for the last row of a sequence, the decision
+// the merge of top-k row r by the MC_T threads: the row's record (also
+// written to p.rstat) and its kept list; FLAG_BLOCK_MERGE when the CTA's
+// staging overflows (ties)
 template <typename T>
-__device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
+__device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
 {
     const unsigned FULL = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -332,6 +333,17 @@ __device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
         st.flags |= FLAG_BLOCK_MERGE;  // ties: more candidates than staged; the decision grid merges
     }
     if (tid == 0) p.rstat[r] = st;
+    return st;
+}
+
+// the merge of top-k row r; then the sequence ticket and, for the last row of
+// a sequence, the decision
+template <typename T>
+__device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const RowRef rr = row_ref(p, r);
+    merge_row_topk_core<T>(p, r, sm);
     // sequence ticket: the barrier orders every thread's writes before thread
     // 0's fence, which makes them visible before the ticket is taken
     ssync();
@@ -361,6 +373,7 @@ __global__ void __launch_bounds__(MC_T, 8) k_merge_cand(const Params p)
 {
     __shared__ McSmem sm;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream grid has completed
+    if (exit_skip(p)) return;
     // the decision grid may be scheduled now; it waits for this grid's end
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int r = blockIdx.x;

@@ -1229,6 +1229,7 @@ __device__ void finish_row(const Params& p, int r, const RowRef& rr, const T* ro
 template <typename T, bool VEC, int MODE>
 __global__ void __launch_bounds__(NT, 4) k_rows(const Params p)
 {
+    if (exit_skip(p)) return;
     __shared__ float s_redf[NT / 32 + 1];
     __shared__ double s_redd[NT / 32 + 1];
     using G = SegGeom<T, NT>;
@@ -1273,6 +1274,7 @@ constexpr int STREAM_SMEM = NSTAGE * SEG_BYTES;
 template <typename T, int MODE>
 __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
 {
+    if (exit_skip(p)) return;
     extern __shared__ __align__(128) unsigned char smem_ring[];  // NSTAGE x SEG_BYTES
     __shared__ Ring ring;
     __shared__ float s_redf[NS / 32 + 1];
@@ -1369,6 +1371,7 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 {
     extern __shared__ __align__(16) unsigned char smem_scratch[];  // SCRATCH_BYTES
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream grid has completed
+    if (exit_skip(p)) return;
     const int r = blockIdx.x;
     const RowRef rr = row_ref(p, r);
     if (!rr.valid) {
@@ -1384,6 +1387,7 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 
 #include "sv_warp.cuh"
 #include "sv_mcand.cuh"
+#include "sv_exit.cuh"
 
 namespace sv {
 

@@ -217,6 +217,7 @@ __device__ unsigned long long segment_pass(const DenseJob& J, float c, int V, in
 template <typename T>
 __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
 {
+    if (exit_skip(p)) return;
     using G = SampleGeom<T>;
     __shared__ unsigned long long s_red[NT / 32 + 1];
     __shared__ unsigned long long s_part[4 * (NT / 32)];
@@ -375,6 +376,7 @@ __global__ void __launch_bounds__(NT) k_probs(const Params p)
 template <typename T>
 __global__ void __launch_bounds__(NT) k_alpha(const Params p)
 {
+    if (exit_skip(p)) return;
     __shared__ unsigned long long s_red[NT / 32 + 1];
     const int K = p.Kmax;
     const int b = blockIdx.x / K, j = blockIdx.x - b * K;

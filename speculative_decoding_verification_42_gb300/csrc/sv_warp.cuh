@@ -717,6 +717,7 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
 {
     extern __shared__ __align__(16) unsigned char smem_w[];
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the stream grid has completed
+    if (exit_skip(p)) return;
     // the decision grid may be scheduled now; it waits for this grid's end
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const unsigned FULL = 0xffffffffu;
@@ -789,6 +790,7 @@ __global__ void __launch_bounds__(NT) k_decide(const Params p)
     extern __shared__ __align__(16) unsigned char smem_scratch[];  // SCRATCH_BYTES
     __shared__ int s_done;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the merge grid has completed
+    if (exit_skip(p)) return;
     const int b = blockIdx.x;
     const int kb = seq_k(p, b);
     if (!k_ok(p, kb)) return;  // reported by the merge grid

@@ -37,7 +37,7 @@ def oracle_tokens(orc, w, *, draft_kind=None, delta=DELTA):
     return toks, margin
 
 
-def run_gpu(w, toks, *, verifier=None, seed=None, round=None, repeat=1):
+def run_gpu(w, toks, *, verifier=None, seed=None, round=None, repeat=1, early_exit=False):
     import torch
     import speculative_decoding_verification_42_gb300 as sv
     target = to_device(w.target)
@@ -53,7 +53,8 @@ def run_gpu(w, toks, *, verifier=None, seed=None, round=None, repeat=1):
     for _ in range(repeat):
         out = verifier.run(target, draft, xt, kpr, temperature=w.temperature, top_k=w.top_k,
                            top_p=w.top_p, seed=w.seed if seed is None else seed,
-                           round=w.round if round is None else round, alpha=True)
+                           round=w.round if round is None else round, alpha=True,
+                           early_exit=early_exit)
         torch.cuda.synchronize()
         outs.append({k: v.cpu().numpy() for k, v in out.items()})
     if own:
@@ -68,8 +69,11 @@ def run_oracle(orc, w, toks, b_begin=0, b_end=None, delta=DELTA):
                       round=w.round, delta=delta, b_begin=b_begin, b_end=b_end)
 
 
-def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL):
-    """Assert parity on the sequences ``rows``; returns the near-tie count."""
+def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL, early_exit=False):
+    """Assert parity on the sequences ``rows``; returns the near-tie count.
+    early_exit: the per-slot outputs exist only for the positions read (up to
+    the first rejection): they are compared there and must be NaN beyond;
+    alpha is not computed."""
     import oracle as O
     rows = np.arange(w.B) if rows is None else np.asarray(rows)
     near = (o["margin_accept"] < delta) | (o["margin_topp"] < delta) | (o["margin_cdf"] < delta)
@@ -93,7 +97,20 @@ def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL):
         assert g["num_accepted"][b] == o["num_accepted"][b], (
             b, g["num_accepted"][b], o["num_accepted"][b], o["margin_accept"][b])
         np.testing.assert_array_equal(g["tokens"][b], o["tokens"][b], err_msg=f"sequence {b}")
-        if st_o in (O.ROW_OK, O.ROW_ZERO_RESIDUAL):
+        if st_o in (O.ROW_OK, O.ROW_ZERO_RESIDUAL) and early_exit:
+            n = int(o["num_accepted"][b])  # positions 0..n were read
+            last = min(n + 1, kb)          # drafted slots with p_t / p_d
+            for name in ("p_t_at_draft", "p_d_at_draft"):
+                np.testing.assert_allclose(g[name][b, :last], o[name][b, :last], rtol=prob_rtol,
+                                           atol=PROB_ATOL, err_msg=f"{name} sequence {b}")
+                assert np.all(np.isnan(g[name][b, last:])), (name, b)
+            np.testing.assert_allclose(g["target_lse"][b, :n + 1], o["target_lse"][b, :n + 1],
+                                       rtol=LSE_RTOL, atol=LSE_ATOL, err_msg=f"lse sequence {b}")
+            assert np.all(np.isnan(g["target_lse"][b, n + 1:]))
+            np.testing.assert_allclose(g["residual_mass"][b], o["residual_mass"][b],
+                                       rtol=prob_rtol, atol=1e-7)
+            assert np.all(np.isnan(g["alpha"][b]))
+        elif st_o in (O.ROW_OK, O.ROW_ZERO_RESIDUAL):
             if "p_t_at_draft" in g:
                 # a row whose nucleus boundary lies inside the window may keep one
                 # boundary token more or less: its probabilities are not compared

@@ -206,6 +206,60 @@ def test_greedy_draft_sampler(orc):
     np.testing.assert_array_equal(g, want)
 
 
+# ------------------------------------------------------ early-exit verify --
+# The rows after the first rejection are not read: the same tokens, lengths
+# and statuses as the full verify; p_t / p_d / lse only at the positions read.
+@pytest.mark.parametrize("V,dtype,B,K,knobs", [
+    (128256, "bf16", 24, 8, dict(top_k=50, temperature=0.7)),
+    (32000, "f32", 40, 6, dict(top_k=20, top_p=0.9)),
+    (50000, "bf16", 30, 5, dict(top_k=1, temperature=1.3)),
+    (20000, "bf16", 20, 7, dict(temperature=0.0)),           # greedy: no draft row read
+])
+def test_early_exit(orc, V, dtype, B, K, knobs):
+    w = make_workload(f"exit V={V}", B=B, K_max=K, V=V, dtype=dtype, target_std=3.0, peaks=10,
+                      peak_height=6.0, draft_noise_std=1.0, ragged_k=(0, K), seed=V + 3, **knobs)
+    toks, _ = oracle_tokens(orc, w)
+    g = run_gpu(w, toks, early_exit=True)
+    o = run_oracle(orc, w, toks)
+    n_near = compare(g, o, w, toks, early_exit=True)
+    assert n_near <= max(1, 0.05 * w.B)
+    assert (o["num_accepted"] < w.k_per_row).any()  # some sequences stop early
+
+
+def test_early_exit_matches_full(orc):
+    """Early exit and the full verify take the same decisions (heavy ties
+    included: rows whose candidates overflow send the batch through the
+    regular pipeline)."""
+    from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
+    for tied in (False, True):
+        w = make_workload("exit vs full", B=16, K_max=6, V=30000, dtype="bf16", target_std=1.5,
+                          draft_noise_std=0.7, seed=61, top_k=60, ragged_k=(0, 6))
+        if tied:
+            w.target = f32_to_bf16_bits(np.round(bf16_bits_to_f32(w.target)))
+            w.draft = f32_to_bf16_bits(np.round(bf16_bits_to_f32(w.draft)))
+        toks, _ = oracle_tokens(orc, w)
+        e = run_gpu(w, toks, early_exit=True)
+        f = run_gpu(w, toks)
+        for k in ("tokens", "num_accepted", "row_status"):
+            np.testing.assert_array_equal(e[k], f[k], err_msg=f"{k} tied={tied}")
+
+
+def test_early_exit_refusals(orc):
+    """Bad K, bad tokens and a non-finite row before the first rejection."""
+    from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
+    w = make_workload("exit refusals", B=6, K_max=4, V=8192, dtype="bf16", seed=62, top_k=30)
+    toks, _ = oracle_tokens(orc, w)
+    toks[1, 0] = w.V                  # a token outside the vocabulary
+    w.k_per_row[2] = w.K_max + 1      # K_b out of range
+    t = bf16_bits_to_f32(w.target)
+    t[3, 0, 17] = np.nan              # position 0 of sequence 3 is always read
+    w.target = f32_to_bf16_bits(t)
+    g = run_gpu(w, toks, early_exit=True)
+    o = run_oracle(orc, w, toks)
+    assert list(g["row_status"][1:4]) == [orc.ROW_BAD_TOKEN, orc.ROW_BAD_K, orc.ROW_NONFINITE]
+    assert compare(g, o, w, toks, early_exit=True) <= 1
+
+
 # ------------------------------------------------------ the five workloads --
 def test_config1_tiny(orc):
     _check(orc, make_config(1))
