@@ -77,9 +77,9 @@ def _traffic(kernel: str, w):
         return None
 
 
-def _workload(n: int):
+def _workload(n: int, batch: int | None = None):
     from workloads import make_config
-    return make_config(n)
+    return make_config(n) if not batch else make_config(n, B=batch)
 
 
 def _wl_config(w, n_rot):
@@ -233,7 +233,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    w = _workload(args.config)
+    w = _workload(args.config, args.batch)
     fused = w.hidden is not None
     per_step = max(1, args.ref_seq)
     if fused:
@@ -327,7 +327,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
 
     sv.load_library()
-    w = _workload(args.config)
+    w = _workload(args.config, args.batch)
 
     def to_dev(a):
         if a.dtype == np.uint16:
@@ -376,7 +376,7 @@ def run_gpu(args):
     def step(i, o):
         c = i % ROTATE
         return ver.run(target[c], draft[c], toks, kpr, out=o, debug=False,
-                       w_vocab=wv if fused else None, **knobs)
+                       w_vocab=wv if fused else None, early_exit=args.early_exit, **knobs)
 
     out = step(0, None)
     for i in range(max(3, args.warmup)):
@@ -441,6 +441,15 @@ def run_gpu(args):
         bytes_step = (w.hidden.size + w.w_vocab.size) * 2 + M * w.V * 4
         flops = 2.0 * M * H * w.V
         kernel = "k_lmhead"
+    elif args.early_exit:
+        # the rows actually read: target rows 0..j*, draft rows 0..min(j*, K_b - 1)
+        na = out["num_accepted"].cpu().numpy().astype(np.int64)
+        kb = w.k_per_row.astype(np.int64)
+        es = 2 if w.dtype == "bf16" else 4
+        d_rows = 0 if (w.draft_kind == "probs" or w.temperature == 0) else int(np.minimum(na + 1, kb).sum())
+        bytes_step = int((na + 1).sum() + d_rows) * w.V * es
+        flops = None
+        kernel = "k_verify_exit"
     else:
         bytes_step = w.logit_bytes()
         flops = None
@@ -509,6 +518,11 @@ def run_gpu(args):
             cpu = cpu_baseline(w, toks.cpu().numpy(), seconds_target=args.cpu_seconds)
     cfg = _wl_config(w, ROTATE)
     cfg["config_id"] = args.config
+    if args.batch:
+        cfg["workload"] += f" (B overridden to {w.B})"
+    if args.early_exit:
+        cfg["mode"] = ("early exit: rows read only up to each sequence's first rejection; "
+                       "roofline bytes are the rows read")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -562,6 +576,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seq", type=int, default=1,
                     help="reference arm: sequences verified by the oracle per step")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="time spec_verify_run_early_exit (top-k rows of logits)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="reference arm: stop the timed loop after this much oracle time")
     args = ap.parse_args(argv)
