@@ -24,7 +24,7 @@
 
 namespace sv {
 
-constexpr int EXIT_CTAS_PER_SM = 2;
+constexpr int EXIT_CTAS_PER_SM = 3;
 
 // verdicts of the compute warps to the producer
 enum : int { EXIT_GO = 1, EXIT_STOP = 0 };
