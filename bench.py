@@ -77,6 +77,22 @@ def _traffic(kernel: str, w):
         return None
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, steps: int, world: int, ms: float) -> float:
+    """Units per second of the whole job: every rank verifies its own batch
+    (replicas, weak scaling) and the job takes the slowest rank's time."""
+    return units_per_rank * steps * world / (ms / 1e3)
+
+
 def _workload(n: int, batch: int | None = None):
     from workloads import make_config
     return make_config(n) if not batch else make_config(n, B=batch)
@@ -427,13 +443,10 @@ def run_gpu(args):
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     mean_step_ms = sum(step_ms) / K
     mean_kern_ms = sum(kern_ms) / K
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     rows = w.rows()
-    value = rows * K * world / (total_ms / 1e3)
+    value = whole_job_rate(rows, K, world, total_ms)
     peak, peak_src = _peaks()
     if fused:
         # the LM head: reads H and W, writes the fp32 logits
@@ -493,15 +506,11 @@ def run_gpu(args):
             e2e_step(i)
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        if dist:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
         h2d = (h_target.numel() * h_target.element_size() + h_draft.numel() * h_draft.element_size()
                + h_toks.numel() * 4 + h_kpr.numel() * 4)
         d2h = h_out_t.numel() * 4 + h_out_n.numel() * 4
-        e2e = {"value": rows * args.e2e_steps * world / (e_ms / 1e3), "unit": UNIT,
+        e2e = {"value": whole_job_rate(rows, args.e2e_steps, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
 
