@@ -260,9 +260,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, EXIT_CTAS_PER_SM) k_verify_exi
                             seg, r, tid, [] { ssync(); }, s_redf, s_redd);
                     }
                     ssync();  // every compute thread is done with the stage
+                    // s_fail only ever goes from 0 to 1, so every thread reads
+                    // the same value after the barrier
                     failed = *(volatile int*)&s_fail != 0;
                     if (tid == 0 && !failed) mbar_arrive(&ring.empty[s]);
-                    ssync();  // every thread has read s_fail
                 }
                 // the row's chunk keys are written by this CTA: merge it
                 __threadfence_block();
