@@ -33,8 +33,6 @@ struct spec_verify {
     unsigned long long* job_seg;
     unsigned long long* job_part;
     unsigned* job_ticket;
-    unsigned long long* grab;
-    unsigned* done;
     unsigned* err;
     unsigned* seq_done;
     unsigned* exit_flag;  // early exit: a sequence was left to the regular pipeline
@@ -107,8 +105,6 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.job_ticket = h->job_ticket;
     p.nseg_sample = h->nseg_sample;
     p.chunk_stride = h->chunk_stride;
-    p.grab = h->grab;
-    p.done = h->done;
     p.err = h->err;
     p.seq_done = h->seq_done;
 }
@@ -150,8 +146,6 @@ size_t layout_workspace(spec_verify* h, void* base)
     const size_t o_jseg = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample);
     const size_t o_jpart = take(sizeof(unsigned long long) * h->jobs_cap * h->nseg_sample * SAMPLE_PARTS);
     const size_t o_jt = take(sizeof(unsigned) * h->jobs_cap);
-    const size_t o_grab = take(sizeof(unsigned long long));
-    const size_t o_done = take(sizeof(unsigned));
     const size_t o_err = take(sizeof(unsigned));
     const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
     const size_t o_xf = take(sizeof(unsigned));
@@ -172,8 +166,6 @@ size_t layout_workspace(spec_verify* h, void* base)
         h->job_seg = (unsigned long long*)(b + o_jseg);
         h->job_part = (unsigned long long*)(b + o_jpart);
         h->job_ticket = (unsigned*)(b + o_jt);
-        h->grab = (unsigned long long*)(b + o_grab);
-        h->done = (unsigned*)(b + o_done);
         h->err = (unsigned*)(b + o_err);
         h->seq_done = (unsigned*)(b + o_sd);
         h->exit_flag = (unsigned*)(b + o_xf);
@@ -549,7 +541,7 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
     if (cudaMemsetAsync(h.row_ticket, 0, tickets, cs) != cudaSuccess ||
         cudaMemsetAsync(h.seq_ticket, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h.job_ticket, 0, sizeof(unsigned) * (size_t)h.jobs_cap, cs) != cudaSuccess ||
-        cudaMemsetAsync(h.grab, 0, 256 * 3, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.err, 0, sizeof(unsigned), cs) != cudaSuccess ||
         cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return spec_verify_run(&h, in, s, out, stream);
