@@ -538,6 +538,22 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// the same copy with an L2 evict-first policy (from l2_evict_first()): data
+// read once does not push out what later kernels read back
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_1d_once(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                 uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol) : "memory");
+}
+
 // launchers (defined in the .cu files)
 cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_t s);

@@ -26,8 +26,9 @@ constexpr int MC_T = NS;         // threads of a row's CTA (its barrier is ssync
 constexpr int MC_CAP = 256;      // candidates a row can stage
 constexpr int MCG_U4 = 4;        // 16-byte words of chunk keys per thread (8 keys each)
 constexpr int MCG_QCAP = 256;    // qualifying chunks a row can stage
-constexpr int MCG_LPT = 4;       // chunk words per thread per load round
+constexpr int MCG_LPT = 8;       // chunk words per thread per load round
 constexpr int MCG_HB = 512;      // histogram bins (keys below the row's largest chunk key)
+constexpr int MCG_QFAST = MC_T * MCG_LPT * 16 / CHUNK_BYTES;  // chunks one gather round reads
 constexpr int MCG_BPT = MCG_HB / MC_T;  // bins a thread sums
 constexpr int MC_STAGE = 4 * WM_CAND * 4;  // the decision's staged kept lists
 static_assert(CAND_TOPK_MAX <= MC_T, "one kept rank per thread; k threads bound the k-th key");
@@ -113,9 +114,12 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
     const uint4* ksrc = reinterpret_cast<const uint4*>(p.chunk + (int64_t)r * p.chunk_stride);
     const int nch = p.nchunk;
     uint4 kw[MCG_U4];  // word g holds keys 8 (g MC_T + tid) .. + 7
+    auto load_keys = [&]() {
 #pragma unroll
-    for (int g = 0; g < MCG_U4; ++g)
-        kw[g] = (g * MC_T + tid) * 8 < nch ? __ldcg(ksrc + g * MC_T + tid) : make_uint4(0, 0, 0, 0);
+        for (int g = 0; g < MCG_U4; ++g)
+            kw[g] = (g * MC_T + tid) * 8 < nch ? __ldcg(ksrc + g * MC_T + tid) : make_uint4(0, 0, 0, 0);
+    };
+    load_keys();
     const RowRef rr = row_ref(p, r);
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     const int x = (rr.j < rr.kb && x_raw >= 0 && x_raw < p.V) ? x_raw : -1;
@@ -196,39 +200,57 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
         }
         ssync();
         const uint32_t tau0 = window_kth(0u);
-        // ---- the k-th largest chunk key from the keys >= tau0
+        // ---- the chunks reaching the bound (at least k of them), compacted,
+        //      read back, and their logits at or above it kept.  tau0 serves
+        //      when it was found, its chunks fit one gather round and their
+        //      candidates the staging; otherwise the bound is raised once, to
+        //      the k-th largest chunk key (counted among the keys >= tau0)
+        auto reaching = [&](uint32_t tau) {
+            uint32_t m = 0u;
 #pragma unroll
-        for (int g = 0; g < MCG_U4; ++g)
+            for (int g = 0; g < MCG_U4; ++g)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t key = key_at(g, i);
-                const uint32_t d = maxkey - key;
-                if (key_in(g, i) && key >= tau0 && d < (uint32_t)MCG_HB) atomicAdd(&sm.u.g.hist[d], 1u);
+                for (int i = 0; i < 8; ++i)
+                    if (key_in(g, i) && key_at(g, i) >= tau) m |= 1u << (g * 8 + i);
+            return m;
+        };
+        auto raise_bound = [&]() {
+#pragma unroll
+            for (int g = 0; g < MCG_U4; ++g)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t key = key_at(g, i);
+                    const uint32_t d = maxkey - key;
+                    if (key_in(g, i) && key >= tau0 && d < (uint32_t)MCG_HB) atomicAdd(&sm.u.g.hist[d], 1u);
+                }
+            ssync();
+            return window_kth(tau0);
+        };
+        uint32_t tau_c = tau0;
+        bool raised = false;
+        // nq, n and the bounds are the same in every thread
+        for (;;) {
+            uint32_t qmask = reaching(tau_c);
+            int nq;
+            int at = mc_excl_scan(__popc(qmask), sm.redi, &nq);
+            if (!raised && (tau0 == 0u || nq > MCG_QFAST)) {
+                tau_c = raise_bound();
+                raised = true;
+                continue;
             }
-        ssync();
-        const uint32_t tau_c = window_kth(tau0);
-        // ---- the chunks reaching it (at least k of them), compacted
-        uint32_t qmask = 0u;
-#pragma unroll
-        for (int g = 0; g < MCG_U4; ++g)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (key_in(g, i) && key_at(g, i) >= tau_c) qmask |= 1u << (g * 8 + i);
-        int nq;
-        int at = mc_excl_scan(__popc(qmask), sm.redi, &nq);
-        while (qmask) {
-            const int bit = __ffs(qmask) - 1;
-            qmask &= qmask - 1u;
-            if (at < MCG_QCAP) sm.u.g.qc[at] = (uint32_t)(((bit >> 3) * MC_T + tid) * 8 + (bit & 7));
-            ++at;
-        }
-        ssync();
-        if (nq <= MCG_QCAP) {
-            // ---- read the chunks back; keep their logits at or above the bound
+            while (qmask) {
+                const int bit = __ffs(qmask) - 1;
+                qmask &= qmask - 1u;
+                if (at < MCG_QCAP) sm.u.g.qc[at] = (uint32_t)(((bit >> 3) * MC_T + tid) * 8 + (bit & 7));
+                ++at;
+            }
+            ssync();
+            if (nq > MCG_QCAP) break;
             constexpr int VW = Vec16<T>::N;
             constexpr int CWD = CHUNK_BYTES / 16;  // words per chunk
             const uint4* rowv = reinterpret_cast<const uint4*>(row);
             const int nw_row = p.V / VW;          // whole words: V s is a multiple of 16 here
+            n = 0;
             for (int w0 = 0; w0 < nq * CWD; w0 += MC_T * MCG_LPT) {
                 uint4 wv[MCG_LPT];
                 int wi[MCG_LPT];
@@ -271,8 +293,15 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
                 }
                 n += tot;
             }
-            ssync();
+            ssync();  // the staging is read; qc and cand may be rewritten
+            if (!raised && n > MC_CAP) {
+                load_keys();  // again: the registers are not held through the gather
+                tau_c = raise_bound();
+                raised = true;
+                continue;
+            }
             staged = true;
+            break;
         }
     }
     if (staged && n >= 1 && n <= MC_CAP) {

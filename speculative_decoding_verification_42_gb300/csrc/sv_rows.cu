@@ -1298,6 +1298,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     if (tid >= NS) {
         // ---------------- producer
         if (tid != NS) return;
+        const uint64_t pol = l2_evict_first();  // the rows are read once; the chunk keys stay in L2
         int k = 0;
         bool failed = false;
         for (int64_t item = blockIdx.x;; item += gridDim.x) {
@@ -1327,7 +1328,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
             const uint32_t bytes =
                 (uint32_t)min((int64_t)SEG_BYTES, row_bytes - (int64_t)seg * SEG_BYTES);
             mbar_arrive_expect_tx(&ring.full[s], bytes);
-            tma_load_1d(smem_ring + (size_t)s * SEG_BYTES, src, bytes, &ring.full[s]);
+            tma_load_1d_once(smem_ring + (size_t)s * SEG_BYTES, src, bytes, &ring.full[s], pol);
             ++k;
         }
         if (failed) {

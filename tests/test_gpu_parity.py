@@ -130,6 +130,23 @@ def test_topk_merge_spike(orc):
     _check(orc, w)
 
 
+def test_topk_merge_clustered_chunks(orc):
+    """Tokens 0..4095 all far above the rest: eight of the row merge's threads
+    own every hot chunk, so the first bound (the k-th largest thread maximum)
+    lies among the cold logits.  Its ~110 chunks fit one gather but hold
+    ~4100 candidates, more than the staging; the bound is raised to the k-th
+    largest chunk key and the chunks read again (~100 candidates)."""
+    from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
+    w = make_workload("clustered", B=4, K_max=3, V=65536, dtype="bf16", target_std=1.0,
+                      draft_noise_std=0.5, seed=91, top_k=50)
+    rng = np.random.default_rng(5)
+    for name in ("target", "draft"):
+        a = bf16_bits_to_f32(getattr(w, name))
+        a[..., :4096] = 6.0 + 4.0 * rng.random(a[..., :4096].shape)
+        setattr(w, name, f32_to_bf16_bits(a))
+    _check(orc, w)
+
+
 def test_topk_merge_draft_probs(orc):
     """Top-k target rows through the row merge, draft given as f32
     probabilities (not streamed)."""
