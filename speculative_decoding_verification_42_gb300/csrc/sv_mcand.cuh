@@ -51,6 +51,10 @@ struct McSmem {
     int stop;                         // first rank the top-p prefix drops
     int flag;                         // this CTA decides the sequence
     float px;
+    int dstate;                       // the decision's head: DECIDE_*
+    int tok;                          // the drawn token
+    unsigned long long redu[MC_T / 32];
+    DecidePending pend;               // the decision's pending sample
 };
 
 // element q (runtime) of a 16-byte word of T
@@ -365,6 +369,82 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
     return st;
 }
 
+// block-wide inclusive prefix sum of one u64 per thread; *total gets the
+// sum.  Two barriers; red may be reused after it returns.
+__device__ __forceinline__ unsigned long long mc_incl_scan_u64(unsigned long long v, unsigned long long* red,
+                                                               unsigned long long* total)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) red[warp] = x;
+    ssync();
+    unsigned long long before = 0ull;
+#pragma unroll
+    for (int w = 0; w < MC_T / 32; ++w) before += w < warp ? red[w] : 0ull;
+    *total = (red[0] + red[1]) + (red[2] + red[3]);
+    ssync();
+    return before + x;
+}
+
+// the pending sample of a decision drawn by the CTA, one kept token per
+// thread (both lists hold at most MC_T): the same fixed-point masses, sums
+// and inverse CDF as warp_sample_list, so the same token.  Every thread gets
+// the token (-1: no mass), *Zfix the first attempt's total and *zero whether
+// the residual had no mass (the row itself was then sampled).
+template <typename T>
+__device__ int mc_sample_list(const Params& p, const DecidePending& pe, McSmem& sm,
+                              unsigned long long* Zfix, bool* zero)
+{
+    const int tid = threadIdx.x;
+    const int n = pe.ts.n_kept;
+    int32_t* ti = reinterpret_cast<int32_t*>(sm.u.stage);
+    float* tv = reinterpret_cast<float*>(sm.u.stage) + MC_T;
+    int32_t* di = reinterpret_cast<int32_t*>(sm.u.stage) + 2 * MC_T;
+    float* dv = reinterpret_cast<float*>(sm.u.stage) + 3 * MC_T;
+    static_assert(4 * MC_T * 4 <= MC_STAGE, "two staged lists fit the stage");
+    const bool res_list = pe.residual && pe.d.kind == 0 && pe.d.st.mode == MODE_LIST;
+    StagedList tl{ti, tv, n}, dl{di, dv, res_list ? pe.d.st.n_kept : 0};
+    if (tid < n) {
+        ti[tid] = __ldcg(p.kept_id + (int64_t)pe.tr * KCAP + tid);
+        tv[tid] = __ldcg(p.kept_l + (int64_t)pe.tr * KCAP + tid);
+    }
+    if (tid < dl.n) {
+        di[tid] = __ldcg(p.kept_id + (int64_t)pe.d.r * KCAP + tid);
+        dv[tid] = __ldcg(p.kept_l + (int64_t)pe.d.r * KCAP + tid);
+    }
+    if (tid == 0) sm.tok = -1;
+    ssync();
+    const float invSt = 1.f / (float)pe.ts.S;
+    const float invSd = (pe.residual && pe.d.kind == 0) ? 1.f / (float)pe.d.st.S : 0.f;
+    *zero = false;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const bool res = pe.residual && attempt == 0;
+        const unsigned long long part =
+            tid < n ? list_r_fix<T>(p, pe.ts, tl, tid, res, pe.d, dl, invSt, invSd) : 0ull;
+        unsigned long long Z;
+        const unsigned long long ex = mc_incl_scan_u64(part, sm.redu, &Z) - part;
+        if (attempt == 0) *Zfix = Z;
+        if (Z == 0ull) {  // the same in every thread
+            if (res) {
+                *zero = true;
+                continue;
+            }
+            return -1;
+        }
+        const unsigned long long t = cdf_target(pe.u, Z);
+        if (ex <= t && t < ex + part) sm.tok = ti[tid];  // one thread at most
+        ssync();
+        return sm.tok;
+    }
+    return -1;
+}
+
 // the merge of top-k row r; then the sequence ticket and, for the last row of
 // a sequence, the decision
 template <typename T>
@@ -374,25 +454,49 @@ __device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
     const RowRef rr = row_ref(p, r);
     merge_row_topk_core<T>(p, r, sm);
     // sequence ticket: the barrier orders every thread's writes before thread
-    // 0's fence, which makes them visible before the ticket is taken
+    // 0's fence, which makes them visible before the ticket is taken; the
+    // last row's second fence, before the next barrier, orders the other
+    // rows' records and lists before any thread of this CTA reads them
     ssync();
     if (tid == 0) {
         __threadfence();
         const int nrows = seq_rows(p, rr.kb);
         const bool last = atomicAdd(&p.seq_ticket[rr.b], 1u) == (unsigned)(nrows - 1);
-        if (last) p.seq_ticket[rr.b] = 0u;
+        if (last) {
+            p.seq_ticket[rr.b] = 0u;
+            __threadfence();
+        }
         sm.flag = last;
     }
     ssync();
     const bool last = sm.flag != 0;
     const int nrows_b = seq_rows(p, rr.kb);
-    if (last && warp == 0 && nrows_b <= 32) {
-        if (lane == 0) __threadfence();
-        __syncwarp();
-        if (warp_decide_lanes<T>(p, rr.b, rr.kb, sm.u.stage)) {
-            __syncwarp();
-            if (lane == 0) p.seq_done[rr.b] = 1u;
+    if (last && nrows_b <= 32) {
+        // warp 0 takes the accept tests; the CTA draws the sample
+        if (warp == 0) {
+            DecidePending pe;
+            const int h = warp_decide_lanes_head<T>(p, rr.b, rr.kb, &pe);
+            if (lane == 0) {
+                sm.dstate = h;
+                if (h == DECIDE_SAMPLE) sm.pend = pe;
+            }
         }
+        ssync();
+        const int h = sm.dstate;
+        if (h == DECIDE_SAMPLE) {
+            const DecidePending& pe = sm.pend;
+            unsigned long long Z;
+            bool zero;
+            if (pe.ts.n_kept <= MC_T && (pe.d.kind != 0 || !pe.residual || pe.d.st.n_kept <= MC_T)) {
+                const int tok = mc_sample_list<T>(p, pe, sm, &Z, &zero);
+                if (tid == 0) decide_finish(p, rr.b, pe, tok, Z, zero);
+            } else if (warp == 0) {
+                const int tok = warp_sample_list<T>(p, pe.tr, pe.ts, pe.residual != 0, pe.d, pe.u, sm.u.stage,
+                                                    &Z, &zero);
+                if (lane == 0) decide_finish(p, rr.b, pe, tok, Z, zero);
+            }
+        }
+        if (h != DECIDE_LEFT && tid == 0) p.seq_done[rr.b] = 1u;
     }
     ssync();  // sm is free again
 }

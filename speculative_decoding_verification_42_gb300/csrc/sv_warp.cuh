@@ -461,12 +461,38 @@ __device__ __forceinline__ RowStat rec_stat(const RecWords& w)
     return r;
 }
 
+// a decision that still needs its sample: the inverse CDF over the kept list
+// of target row tr (its residual against the draft d, or the row itself) at u
+struct DecidePending {
+    int jstar;     // the emitted slot
+    int tr;        // target row slot
+    int residual;  // the residual of a rejection (else the bonus / greedy row)
+    float u;
+    RowStat ts;
+    DraftRef d;
+};
+
+// the outputs of a pending decision once its sample tok is drawn (one thread)
+__device__ __forceinline__ void decide_finish(const Params& p, int b, const DecidePending& pe, int tok,
+                                              unsigned long long Z, bool zero)
+{
+    p.tokens[(int64_t)b * (p.Kmax + 1) + pe.jstar] = tok;
+    p.num_accepted[b] = pe.jstar;
+    if (p.row_status) p.row_status[b] = zero ? ROW_ZERO_RESIDUAL : ROW_OK;
+    if (p.resid_mass) p.resid_mass[b] = pe.residual ? (float)from_fix56(Z) : 0.f;
+    p.jobs[b].kind = JOB_NONE;
+}
+
+enum : int { DECIDE_LEFT = 0, DECIDE_DONE = 1, DECIDE_SAMPLE = 2 };
+
 // the decision of sequence b by one warp when its rows fit one per lane
 // (2 K_b + 1 <= 32): lane i holds row record i (target rows 0..K_b, then
 // draft rows 0..K_b-1) and slot i's drafted token, all loaded in one round;
-// the same arithmetic and outputs as warp_decide
+// the same arithmetic and outputs as warp_decide.  Up to the sample:
+// DECIDE_LEFT (a row needs the decision grid), DECIDE_DONE, or DECIDE_SAMPLE
+// with *pe (the same in every lane) to be drawn and passed to decide_finish
 template <typename T>
-__device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char* stage)
+__device__ int warp_decide_lanes_head(const Params& p, int b, int kb, DecidePending* pe)
 {
     const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -481,7 +507,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
     const bool mine = lane < nrows;
     if (__any_sync(FULL, mine && ((me.flags & FLAG_BLOCK_MERGE) ||
                                   (me.mode == MODE_LIST && me.n_kept > WM_CAND))))
-        return false;
+        return DECIDE_LEFT;
     bool nonf = __any_sync(FULL, mine && (me.flags & FLAG_NONFINITE));
     const bool bad = __any_sync(FULL, lane < kb && (x < 0 || x >= V));
     float q = 1.f;
@@ -504,7 +530,7 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
             if (p.resid_mass) p.resid_mass[b] = NAN;
             p.jobs[b].kind = JOB_NONE;
         }
-        return true;
+        return DECIDE_DONE;
     }
     // accept tests, one slot per lane; the first rejection is the lowest
     // rejecting lane
@@ -552,17 +578,15 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
                                      (drow0 + (int64_t)jstar * V) * (d.kind == 1 ? 4 : (int64_t)sizeof(T)))
                      : nullptr;
     if (ts.mode == MODE_LIST) {
-        unsigned long long Z;
-        bool zero;
-        const int tok = warp_sample_list<T>(p, tr, ts, residual, d, u, stage, &Z, &zero);
-        if (lane == 0) {
-            p.tokens[(int64_t)b * (K + 1) + jstar] = tok;
-            p.num_accepted[b] = jstar;
-            if (p.row_status) p.row_status[b] = zero ? ROW_ZERO_RESIDUAL : ROW_OK;
-            if (p.resid_mass) p.resid_mass[b] = residual ? (float)from_fix56(Z) : 0.f;
-            p.jobs[b].kind = JOB_NONE;
-        }
-    } else if (lane == 0) {
+        pe->jstar = jstar;
+        pe->tr = tr;
+        pe->residual = residual;
+        pe->u = u;
+        pe->ts = ts;
+        pe->d = d;
+        return DECIDE_SAMPLE;
+    }
+    if (lane == 0) {
         p.tokens[(int64_t)b * (K + 1) + jstar] = -1;
         p.num_accepted[b] = jstar;
         if (p.row_status) p.row_status[b] = ROW_OK;
@@ -576,8 +600,24 @@ __device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char*
         jb.u = u;
         p.jobs[b] = jb;
     }
+    return DECIDE_DONE;
+}
+
+// the decision of sequence b by one warp (rows one per lane) with the warp's
+// own sample; false leaves it to the decision grid
+template <typename T>
+__device__ bool warp_decide_lanes(const Params& p, int b, int kb, unsigned char* stage)
+{
+    DecidePending pe;
+    const int h = warp_decide_lanes_head<T>(p, b, kb, &pe);
+    if (h != DECIDE_SAMPLE) return h == DECIDE_DONE;
+    unsigned long long Z;
+    bool zero;
+    const int tok = warp_sample_list<T>(p, pe.tr, pe.ts, pe.residual != 0, pe.d, pe.u, stage, &Z, &zero);
+    if ((threadIdx.x & 31) == 0) decide_finish(p, b, pe, tok, Z, zero);
     return true;
 }
+
 
 // true when the warp decided sequence b; false leaves it to the decision grid
 // (a row of it needs the block merge)
