@@ -35,7 +35,7 @@ static_assert(CAND_TOPK_MAX <= MC_T, "one kept rank per thread; k threads bound 
 static_assert(MC_T * MCG_U4 * 8 >= 4096, "the merge holds every chunk key of a warp-merge row");
 static_assert(MC_T == 128, "the block sums add four warp sums");
 
-struct McSmem {
+struct __align__(16) McSmem {
     union {
         struct {
             uint32_t hist[MCG_HB];    // chunk keys at (largest key - bin)
@@ -56,6 +56,18 @@ struct McSmem {
     unsigned long long redu[MC_T / 32];
     DecidePending pend;               // the decision's pending sample
 };
+// after the merge, u, cand and ord (one 8 KB span) stage the kept lists of
+// the deciding CTA's sequence
+constexpr int MC_PRE_BYTES = MC_STAGE + 2 * MC_CAP * 8;
+static_assert(offsetof(McSmem, u) == 0 && sizeof(McSmem::u) == MC_STAGE && offsetof(McSmem, cand) == MC_STAGE &&
+                  offsetof(McSmem, ord) == MC_STAGE + MC_CAP * 8,
+              "u, cand and ord are one span at the start");
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // element q (runtime) of a 16-byte word of T
 template <typename T> __device__ __forceinline__ float word_elem_rt(uint4 w, int q);
@@ -392,34 +404,18 @@ __device__ __forceinline__ unsigned long long mc_incl_scan_u64(unsigned long lon
     return before + x;
 }
 
-// the pending sample of a decision drawn by the CTA, one kept token per
-// thread (both lists hold at most MC_T): the same fixed-point masses, sums
-// and inverse CDF as warp_sample_list, so the same token.  Every thread gets
-// the token (-1: no mass), *Zfix the first attempt's total and *zero whether
-// the residual had no mass (the row itself was then sampled).
+// the pending sample of a decision drawn by the CTA from staged lists, one
+// kept token per thread (both lists hold at most MC_T): the same fixed-point
+// masses, sums and inverse CDF as warp_sample_list, so the same token.
+// sm.tok must be -1 before the barrier that ordered the staging.  Every
+// thread gets the token (-1: no mass), *Zfix the first attempt's total and
+// *zero whether the residual had no mass (the row itself was then sampled).
 template <typename T>
-__device__ int mc_sample_list(const Params& p, const DecidePending& pe, McSmem& sm,
-                              unsigned long long* Zfix, bool* zero)
+__device__ int mc_sample_staged(const Params& p, const DecidePending& pe, const StagedList& tl,
+                                const StagedList& dl, McSmem& sm, unsigned long long* Zfix, bool* zero)
 {
     const int tid = threadIdx.x;
-    const int n = pe.ts.n_kept;
-    int32_t* ti = reinterpret_cast<int32_t*>(sm.u.stage);
-    float* tv = reinterpret_cast<float*>(sm.u.stage) + MC_T;
-    int32_t* di = reinterpret_cast<int32_t*>(sm.u.stage) + 2 * MC_T;
-    float* dv = reinterpret_cast<float*>(sm.u.stage) + 3 * MC_T;
-    static_assert(4 * MC_T * 4 <= MC_STAGE, "two staged lists fit the stage");
-    const bool res_list = pe.residual && pe.d.kind == 0 && pe.d.st.mode == MODE_LIST;
-    StagedList tl{ti, tv, n}, dl{di, dv, res_list ? pe.d.st.n_kept : 0};
-    if (tid < n) {
-        ti[tid] = __ldcg(p.kept_id + (int64_t)pe.tr * KCAP + tid);
-        tv[tid] = __ldcg(p.kept_l + (int64_t)pe.tr * KCAP + tid);
-    }
-    if (tid < dl.n) {
-        di[tid] = __ldcg(p.kept_id + (int64_t)pe.d.r * KCAP + tid);
-        dv[tid] = __ldcg(p.kept_l + (int64_t)pe.d.r * KCAP + tid);
-    }
-    if (tid == 0) sm.tok = -1;
-    ssync();
+    const int n = tl.n;
     const float invSt = 1.f / (float)pe.ts.S;
     const float invSd = (pe.residual && pe.d.kind == 0) ? 1.f / (float)pe.d.st.S : 0.f;
     *zero = false;
@@ -438,11 +434,38 @@ __device__ int mc_sample_list(const Params& p, const DecidePending& pe, McSmem& 
             return -1;
         }
         const unsigned long long t = cdf_target(pe.u, Z);
-        if (ex <= t && t < ex + part) sm.tok = ti[tid];  // one thread at most
+        if (ex <= t && t < ex + part) sm.tok = tl.ids[tid];  // one thread at most
         ssync();
         return sm.tok;
     }
     return -1;
+}
+
+// the same, staging the two lists from global memory first
+template <typename T>
+__device__ int mc_sample_list(const Params& p, const DecidePending& pe, McSmem& sm,
+                              unsigned long long* Zfix, bool* zero)
+{
+    const int tid = threadIdx.x;
+    const int n = pe.ts.n_kept;
+    int32_t* ti = reinterpret_cast<int32_t*>(sm.u.stage);
+    float* tv = reinterpret_cast<float*>(sm.u.stage) + MC_T;
+    int32_t* di = reinterpret_cast<int32_t*>(sm.u.stage) + 2 * MC_T;
+    float* dv = reinterpret_cast<float*>(sm.u.stage) + 3 * MC_T;
+    static_assert(4 * MC_T * 4 <= MC_STAGE, "two staged lists fit the stage");
+    const bool res_list = pe.residual && pe.d.kind == 0 && pe.d.st.mode == MODE_LIST;
+    const StagedList tl{ti, tv, n}, dl{di, dv, res_list ? pe.d.st.n_kept : 0};
+    if (tid < n) {
+        ti[tid] = __ldcg(p.kept_id + (int64_t)pe.tr * KCAP + tid);
+        tv[tid] = __ldcg(p.kept_l + (int64_t)pe.tr * KCAP + tid);
+    }
+    if (tid < dl.n) {
+        di[tid] = __ldcg(p.kept_id + (int64_t)pe.d.r * KCAP + tid);
+        dv[tid] = __ldcg(p.kept_l + (int64_t)pe.d.r * KCAP + tid);
+    }
+    if (tid == 0) sm.tok = -1;
+    ssync();
+    return mc_sample_staged<T>(p, pe, tl, dl, sm, Zfix, zero);
 }
 
 // the merge of top-k row r; then the sequence ticket and, for the last row of
@@ -472,14 +495,33 @@ __device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
     const bool last = sm.flag != 0;
     const int nrows_b = seq_rows(p, rr.kb);
     if (last && nrows_b <= 32) {
-        // warp 0 takes the accept tests; the CTA draws the sample
+        // warp 0 takes the accept tests while the other warps stage the kept
+        // list of every row of the sequence (when they fit); then the CTA
+        // draws the sample.  A list holds at most top_k tokens.
+        const int kb = rr.kb;
+        const int klp = (p.top_k + 3) & ~3;  // a staged list, rounded to 16 bytes
+        const bool pre = 2 * nrows_b * klp * 4 <= MC_PRE_BYTES;
+        int32_t* pid = reinterpret_cast<int32_t*>(&sm);
+        float* pl = reinterpret_cast<float*>(&sm) + nrows_b * klp;
         if (warp == 0) {
             DecidePending pe;
-            const int h = warp_decide_lanes_head<T>(p, rr.b, rr.kb, &pe);
+            const int h = warp_decide_lanes_head<T>(p, rr.b, kb, &pe);
             if (lane == 0) {
                 sm.dstate = h;
+                sm.tok = -1;
                 if (h == DECIDE_SAMPLE) sm.pend = pe;
             }
+        } else if (pre) {
+            const int per = klp / 4;  // 16-byte words of a staged list
+            const int nw = nrows_b * per;
+            for (int e = tid - 32; e < 2 * nw; e += MC_T - 32) {
+                const int half = e >= nw;  // 0: ids, 1: logits
+                const int i = (e - half * nw) / per, q = (e - half * nw) - i * per;
+                const int64_t row = i <= kb ? target_slot(p, rr.b, i) : draft_slot(p, rr.b, i - kb - 1);
+                if (half) cp_async16(pl + i * klp + 4 * q, p.kept_l + row * KCAP + 4 * q);
+                else cp_async16(pid + i * klp + 4 * q, p.kept_id + row * KCAP + 4 * q);
+            }
+            cp_async_wait_all();
         }
         ssync();
         const int h = sm.dstate;
@@ -487,7 +529,15 @@ __device__ void merge_row_topk(const Params& p, int r, McSmem& sm)
             const DecidePending& pe = sm.pend;
             unsigned long long Z;
             bool zero;
-            if (pe.ts.n_kept <= MC_T && (pe.d.kind != 0 || !pe.residual || pe.d.st.n_kept <= MC_T)) {
+            const bool res_list = pe.residual && pe.d.kind == 0 && pe.d.st.mode == MODE_LIST;
+            const int nd = res_list ? pe.d.st.n_kept : 0;
+            if (pre && pe.ts.n_kept <= min(klp, MC_T) && nd <= min(klp, MC_T)) {
+                const int jt = pe.jstar, jd = kb + 1 + pe.jstar;
+                const StagedList tl{pid + jt * klp, pl + jt * klp, pe.ts.n_kept};
+                const StagedList dl{pid + (res_list ? jd : 0) * klp, pl + (res_list ? jd : 0) * klp, nd};
+                const int tok = mc_sample_staged<T>(p, pe, tl, dl, sm, &Z, &zero);
+                if (tid == 0) decide_finish(p, rr.b, pe, tok, Z, zero);
+            } else if (pe.ts.n_kept <= MC_T && nd <= MC_T) {
                 const int tok = mc_sample_list<T>(p, pe, sm, &Z, &zero);
                 if (tid == 0) decide_finish(p, rr.b, pe, tok, Z, zero);
             } else if (warp == 0) {
