@@ -2,11 +2,14 @@
 // one CTA per row slot after the chunk-key stream (included by sv_rows.cu
 // after the streaming kernel and the warp code).
 //
-//  * bound: the k-th largest of the row's 128-byte chunk maxima bounds its
-//    k-th largest logit from below (k chunks each hold a logit at least that
-//    large).  It is found from the chunk keys by counting them in a window of
-//    MCG_HB keys below the largest, after a first bound (the k-th largest of
-//    the threads' own largest keys) has removed all but a few;
+//  * bound: any value that k chunks reach bounds the row's k-th largest
+//    logit from below (each of those chunks holds a logit at least that
+//    large).  The first bound is the k-th largest of the threads' own
+//    largest chunk keys (k <= MC_T threads each hold one), counted in a
+//    window of MCG_HB keys below the row's largest; when it was not found,
+//    or its chunks exceed one gather round, or their candidates the staging,
+//    it is raised once to the k-th largest chunk key (the same count over
+//    the keys at or above the first bound);
 //  * candidates: the chunks reaching the bound are read back from HBM and
 //    their logits at or above it kept, each list compacted with one
 //    block-wide prefix sum;
@@ -15,9 +18,11 @@
 //    then the top-p prefix in rank order; the kept list goes out in ascending
 //    id with M, S and P(x) at the drafted token.
 //
-// The last row of a sequence to be merged decides the sequence (warp 0, the
-// decision of sv_warp.cuh).  Rows with more candidates than the CTA stages
-// (ties), and sequences of more than 32 rows, are left to the decision grid.
+// The last row of a sequence to be merged decides the sequence: warp 0 takes
+// the accept tests (the head of the warp decision of sv_warp.cuh) while the
+// other warps stage the sequence's kept lists, then the CTA draws the sample.
+// Rows with more candidates than the CTA stages (ties), and sequences of more
+// than 32 rows, are left to the decision grid.
 #pragma once
 
 namespace sv {
