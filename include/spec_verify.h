@@ -70,7 +70,7 @@ typedef struct spec_verify* spec_verify_t; /* opaque handle */
 typedef enum {
     SPEC_OK = 0,
     SPEC_ERR_INVALID_ARG = 1, /* a NULL required pointer, a size out of range, a bad knob */
-    SPEC_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement          */
+    SPEC_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement        */
     SPEC_ERR_OOM = 3,         /* workspace allocation failed (create only)              */
     SPEC_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed            */
     SPEC_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait ran out           */
