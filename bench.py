@@ -328,6 +328,216 @@ def run_reference(args):
 # --------------------------------------------------------------------------- #
 # the GB300 arm                                                               #
 # --------------------------------------------------------------------------- #
+L2_BYTES = 129 * 2**20      # GB300 L2, for the rotation / flush decision
+
+
+class Arm:
+    """One workload resident on the device, ready to run verify steps."""
+
+    def __init__(self, sv, torch, w, dev, local, early_exit=False, min_rot=ROTATE):
+        self.sv, self.torch, self.w, self.dev = sv, torch, w, dev
+        self.early_exit = early_exit
+        self.stream = torch.cuda.current_stream(dev)
+        self.kpr = torch.from_numpy(w.k_per_row).to(dev)
+        self.knobs = dict(temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed)
+        self.fused = w.hidden is not None
+        self.wv = None
+
+        def to_dev(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        if self.fused:
+            # the fused round: hidden states x W_vocab, then the verify against
+            # draft probabilities softmax((target logits + noise) / T) (the
+            # workload's recipe, prepared once here); W (2.1 GB) exceeds L2
+            H = w.hidden.shape[1]
+            self.H = H
+            hid = to_dev(w.hidden)
+            self.wv = to_dev(w.w_vocab)
+            logits = torch.empty((w.B * (w.K_max + 1), w.V), dtype=torch.float32, device=dev)
+            sv.spec_lmhead_logits(hid.data_ptr(), self.wv.data_ptr(), logits.shape[0], H, w.V,
+                                  logits.data_ptr(), self.stream.cuda_stream)
+            lg = logits.view(w.B, w.K_max + 1, w.V)[:, :w.K_max]
+            probs = torch.softmax((lg + to_dev(w.draft_noise)) / w.temperature, dim=-1).contiguous()
+            del logits, lg
+            self.ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype="bf16",
+                                   device=local, draft_kind="probs", hidden=H)
+            # drafted tokens x ~ P_d: inputs of the round, drawn once by torch
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(w.seed)
+            toks = torch.multinomial(probs.view(-1, w.V), 1, generator=gen)
+            self.toks = toks.view(w.B, w.K_max).to(torch.int32).contiguous()
+            self.n_rot = 1
+            self.target, self.draft = [hid], [probs]
+            self.l2 = f"every step reads W_vocab ({w.w_vocab.size * 2 / 1e9:.2f} GB) > L2"
+        else:
+            self.target, self.draft = [to_dev(w.target)], [to_dev(w.draft)]
+            step_bytes = w.logit_bytes()
+            # enough copies to exceed L2 twice over, unless that would be absurd
+            # (the tiny workloads take an L2 flush between steps instead)
+            n_rot = max(min_rot, -(-2 * L2_BYTES // step_bytes))
+            self.n_rot = n_rot if n_rot <= 64 else 1
+            for _ in range(self.n_rot - 1):
+                self.target.append(self.target[0].clone())
+                self.draft.append(self.draft[0].clone())
+            self.ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype=w.dtype,
+                                   device=local, draft_kind=w.draft_kind)
+            # drafted tokens: the library's draft-side sampler (tag-1 uniforms)
+            self.toks = self.ver.draft_sample(self.draft[0], self.kpr, **self.knobs)
+            rb = self.n_rot * step_bytes
+            self.l2 = (f"{self.n_rot} rotating input copies ({rb / 1e6:.0f} MB) > L2"
+                       if self.n_rot > 1 else
+                       "L2 flushed between steps (a 256 MB write outside the per-step events)")
+        self.flush = None
+        if self.n_rot == 1 and not self.fused:
+            self.flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+        self.out = None
+        torch.cuda.synchronize()
+        self.out = self.step(0)
+
+    def step(self, i):
+        c = i % self.n_rot
+        return self.ver.run(self.target[c], self.draft[c], self.toks, self.kpr, out=self.out,
+                            debug=False, w_vocab=self.wv, early_exit=self.early_exit,
+                            **self.knobs)
+
+    def kernel_and_bytes(self):
+        """The dominant kernel, its algorithmic bytes per launch, flops (or None)."""
+        w = self.w
+        if self.fused:
+            M = w.B * (w.K_max + 1)
+            return ("k_lmhead", (w.hidden.size + w.w_vocab.size) * 2 + M * w.V * 4,
+                    2.0 * M * self.H * w.V)
+        if self.early_exit:
+            # the rows actually read: target rows 0..j*, draft rows 0..min(j*, K_b - 1)
+            na = self.out["num_accepted"].cpu().numpy().astype(np.int64)
+            kb = w.k_per_row.astype(np.int64)
+            es = 2 if w.dtype == "bf16" else 4
+            d_rows = 0 if (w.draft_kind == "probs" or w.temperature == 0) else \
+                int(np.minimum(na + 1, kb).sum())
+            return "k_verify_exit", int((na + 1).sum() + d_rows) * w.V * es, None
+        return _stage1_kernel(w), w.logit_bytes(), None
+
+    def close(self):
+        self.ver.close()
+
+
+def timed_loop(arm, K, W, dist=None, per_step=False, sample_every=None):
+    """W warm-up steps, then exactly K timed steps between a barrier and a
+    synchronize on both sides.  The library's events around its stage-1
+    kernel go on every sample_every-th step from step 1 on (at least 16 of
+    them when K allows).  per_step: an event pair around every step and an L2
+    flush between steps, outside the pairs (inputs smaller than L2)."""
+    import ctypes
+    import torch
+    sv = arm.sv
+    stream = arm.stream
+    for i in range(max(3, W)):
+        arm.step(i)
+    if sample_every is None:
+        sample_every = max(1, (K - 1) // 16)
+    kev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for i in range(1 if K > 1 else 0, K, sample_every)}
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)] if per_step else []
+    for a, b in list(kev.values()) + sev:  # torch creates the CUDA events on first record
+        a.record(stream)
+        b.record(stream)
+    n_launch = ctypes.c_int32(0)
+    sv.spec_verify_set_profiling(arm.ver.h, None, None, n_launch)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    h0 = time.perf_counter()
+    t_start.record(stream)
+    for i in range(K):
+        pair = kev.get(i)
+        if per_step:
+            arm.flush.zero_()
+            sev[i][0].record(stream)
+        if pair:
+            sv.spec_verify_set_profiling(arm.ver.h, pair[0].cuda_event, pair[1].cuda_event, n_launch)
+        arm.step(i)
+        if pair:
+            sv.spec_verify_set_profiling(arm.ver.h, None, None, n_launch)
+        if per_step:
+            sev[i][1].record(stream)
+        launches += n_launch.value
+    t_end.record(stream)
+    host_s = time.perf_counter() - h0
+    torch.cuda.synchronize()
+    sv.spec_verify_set_profiling(arm.ver.h, None, None, None)
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    if per_step:
+        step_ms = [a.elapsed_time(b) for a, b in sev]
+        total_ms = sum(step_ms)
+    kern_ms = [a.elapsed_time(b) for a, b in kev.values()]
+    return {"total_ms": total_ms, "kern_ms": kern_ms, "launches": launches,
+            "host_us_per_step": 1e6 * host_s / K}
+
+
+def _kstats(kern_ms):
+    ks = sorted(kern_ms)
+    return {"median_us": 1e3 * statistics.median(ks), "mean_us": 1e3 * statistics.fmean(ks),
+            "min_us": 1e3 * ks[0], "max_us": 1e3 * ks[-1], "n": len(ks)}
+
+
+def workload_summary(sv, torch, n, dev, local, steps, warmup, peak):
+    """value, ms_per_step and the stage-1 kernel's fraction of one workload,
+    timed like the headline (its own arm, warm-up and K steps)."""
+    w = _workload(n)
+    arm = Arm(sv, torch, w, dev, local)
+    r = timed_loop(arm, steps, warmup, per_step=arm.flush is not None)
+    kernel, bytes_step, flops = arm.kernel_and_bytes()
+    ks = _kstats(r["kern_ms"])
+    step_us = 1e3 * r["total_ms"] / steps
+    d = {"workload": w.name, "value": w.rows() / (step_us * 1e-6), "unit": UNIT,
+         "ms_per_step": step_us / 1e3, "kernel": kernel,
+         "kernel_us_median": ks["median_us"], "launches_timed": ks["n"],
+         "algorithmic_bytes_per_launch": bytes_step,
+         "frac": bytes_step / (ks["median_us"] * 1e-6) / 1e9 / peak,
+         "step_frac": bytes_step / (step_us * 1e-6) / 1e9 / peak, "l2": arm.l2,
+         "gpu_launches": r["launches"]}
+    if flops:
+        d["tensor_frac"] = flops / (ks["median_us"] * 1e-6) / 1e12 / _tensor_peak()
+        d.update(_verify_stage(arm, step_us, ks["median_us"], peak))
+    arm.close()
+    del arm
+    torch.cuda.empty_cache()
+    return d
+
+
+def _verify_stage(arm, step_us, lm_us, peak):
+    """The fused round's verify stage (the step without the LM head) against
+    the bytes it reads: the LM head's softmax partials, the logits and draft
+    probabilities at the drafted tokens, and the rows the sample reads (the
+    target row j* and the draft row j* after a rejection, the bonus row
+    otherwise)."""
+    w = arm.w
+    na = arm.out["num_accepted"].cpu().numpy().astype(np.int64)
+    kb = w.k_per_row.astype(np.int64)
+    rej = na < kb
+    rows_read = int((1 + rej).sum())
+    nseg = -(-w.V // 256)
+    stats = int((kb + 1).sum()) * nseg * 16
+    at_tokens = int(kb.sum()) * 2 * 4
+    vb = rows_read * w.V * 4 + stats + at_tokens
+    v_us = step_us - lm_us
+    return {"verify_stage": {
+        "us": v_us, "bytes_read": vb, "achieved_gbs": vb / (v_us * 1e-6) / 1e9,
+        "frac": vb / (v_us * 1e-6) / 1e9 / peak,
+        "note": "step minus the LM head's median launch; bytes: the LM head's softmax partials, "
+                "the values at the drafted tokens and the sampled rows (latency-bound)"}}
+
+
 def run_gpu(args):
     import torch
     import speculative_decoding_verification_42_gb300 as sv
@@ -344,138 +554,37 @@ def run_gpu(args):
 
     sv.load_library()
     w = _workload(args.config, args.batch)
-
-    def to_dev(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(a).to(dev)
-
-    stream = torch.cuda.current_stream(dev)
-    kpr = torch.from_numpy(w.k_per_row).to(dev)
-    knobs = dict(temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed)
-    fused = w.hidden is not None
-    if fused:
-        # the fused round: hidden states x W_vocab, then the verify against
-        # draft probabilities softmax((target logits + noise) / T) (the
-        # workload's recipe, prepared once here); W (2.1 GB) exceeds L2
-        H = w.hidden.shape[1]
-        hid = to_dev(w.hidden)
-        wv = to_dev(w.w_vocab)
-        logits = torch.empty((w.B * (w.K_max + 1), w.V), dtype=torch.float32, device=dev)
-        sv.spec_lmhead_logits(hid.data_ptr(), wv.data_ptr(), logits.shape[0], H, w.V,
-                              logits.data_ptr(), stream.cuda_stream)
-        lg = logits.view(w.B, w.K_max + 1, w.V)[:, :w.K_max]
-        probs = torch.softmax((lg + to_dev(w.draft_noise)) / w.temperature, dim=-1).contiguous()
-        del logits, lg
-        ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype="bf16", device=local,
-                          draft_kind="probs", hidden=H)
-        # drafted tokens x ~ P_d: inputs of the round, drawn once by torch
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(w.seed)
-        toks = torch.multinomial(probs.view(-1, w.V), 1, generator=gen)
-        toks = toks.view(w.B, w.K_max).to(torch.int32).contiguous()
-        target = [hid] * ROTATE
-        draft = [probs] * ROTATE
-    else:
-        target = [to_dev(w.target)]
-        draft = [to_dev(w.draft)]
-        for _ in range(ROTATE - 1):
-            target.append(target[0].clone())
-            draft.append(draft[0].clone())
-        ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype=w.dtype, device=local,
-                          draft_kind=w.draft_kind)
-        # drafted tokens: the library's draft-side sampler (tag-1 uniforms)
-        toks = ver.draft_sample(draft[0], kpr, **knobs)
-    torch.cuda.synchronize()
-    out = None
-
-    def step(i, o):
-        c = i % ROTATE
-        return ver.run(target[c], draft[c], toks, kpr, out=o, debug=False,
-                       w_vocab=wv if fused else None, early_exit=args.early_exit, **knobs)
-
-    out = step(0, None)
-    for i in range(max(3, args.warmup)):
-        step(i, out)
-    torch.cuda.synchronize()
-
-    # the library records a pair of events around its stage-1 stream kernel
-    # (the kernel that reads the logits) and reports its kernel count per
-    # run.  The events go on every SAMPLE-th step only: an event recorded
-    # between two kernels keeps the second from being scheduled while the
-    # first drains, so the other steps run as a caller's loop would.
-    import ctypes
-    K = args.steps
-    SAMPLE = 32
-    n_launch = ctypes.c_int32(0)
-    kev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for i in range(0, K, SAMPLE)}
-    for a, b in kev.values():  # torch creates the CUDA events on first record
-        a.record(stream)
-        b.record(stream)
-    torch.cuda.synchronize()
     try:
         gpu_sel = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_sel = str(local)
+    # the clock sampler starts before the warm-up, so that no idle gap sits
+    # between the warm-up and the timed steps
     sampler = ClockSampler(gpu_sel) if rank == 0 else None
     if sampler:
         sampler.start()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    launches = 0
-    sv.spec_verify_set_profiling(ver.h, None, None, n_launch)
-    t_start.record(stream)
-    for i in range(K):
-        pair = kev.get(i)
-        if pair:
-            sv.spec_verify_set_profiling(ver.h, pair[0].cuda_event, pair[1].cuda_event, n_launch)
-        step(i, out)
-        if pair:
-            sv.spec_verify_set_profiling(ver.h, None, None, n_launch)
-        launches += n_launch.value
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    sv.spec_verify_set_profiling(ver.h, None, None, None)
-    if dist:
-        dist.barrier()
+    arm = Arm(sv, torch, w, dev, local, early_exit=args.early_exit)
+    K = args.steps
+    r = timed_loop(arm, K, args.warmup, dist=dist)
     clocks = sampler.stop() if sampler else None
-    total_ms = t_start.elapsed_time(t_end)
-    kern_ms = [a.elapsed_time(b) for a, b in kev.values()]
-    mean_step_ms = total_ms / K
-    mean_kern_ms = sum(kern_ms) / len(kern_ms)
-    total_ms = max_over_ranks(total_ms, dist, dev)
-
+    total_ms = max_over_ranks(r["total_ms"], dist, dev)
+    kern_ms = r["kern_ms"]
+    ks = _kstats(kern_ms)
+    mean_step_ms = r["total_ms"] / K
     rows = w.rows()
     value = whole_job_rate(rows, K, world, total_ms)
     peak, peak_src = _peaks()
-    if fused:
-        # the LM head: reads H and W, writes the fp32 logits
-        M = w.B * (w.K_max + 1)
-        bytes_step = (w.hidden.size + w.w_vocab.size) * 2 + M * w.V * 4
-        flops = 2.0 * M * H * w.V
-        kernel = "k_lmhead"
-    elif args.early_exit:
-        # the rows actually read: target rows 0..j*, draft rows 0..min(j*, K_b - 1)
-        na = out["num_accepted"].cpu().numpy().astype(np.int64)
-        kb = w.k_per_row.astype(np.int64)
-        es = 2 if w.dtype == "bf16" else 4
-        d_rows = 0 if (w.draft_kind == "probs" or w.temperature == 0) else int(np.minimum(na + 1, kb).sum())
-        bytes_step = int((na + 1).sum() + d_rows) * w.V * es
-        flops = None
-        kernel = "k_verify_exit"
-    else:
-        bytes_step = w.logit_bytes()
-        flops = None
-        kernel = _stage1_kernel(w)
-    achieved = bytes_step / (mean_kern_ms / 1e3) / 1e9
+    kernel, bytes_step, flops = arm.kernel_and_bytes()
+    achieved = bytes_step / (ks["median_us"] * 1e-6) / 1e9
 
-    # end to end: host buffers through the same call, copies inside the timed region
+    # end to end: host buffers through the same call, copies inside the timed
+    # region; the inputs go in on two copy streams (target and draft on
+    # separate copy engines), the compute stream waits for both
     e2e = None
     if args.e2e_steps > 0:
+        out = arm.out
+        target, draft, toks, kpr = arm.target, arm.draft, arm.toks, arm.kpr
+        stream = arm.stream
         h_target = torch.empty(target[0].shape, dtype=target[0].dtype, pin_memory=True)
         h_draft = torch.empty(draft[0].shape, dtype=draft[0].dtype, pin_memory=True)
         h_target.copy_(target[0])
@@ -486,15 +595,35 @@ def run_gpu(args):
         h_out_n = torch.empty(out["num_accepted"].shape, dtype=torch.int32, pin_memory=True)
         d_toks = torch.empty_like(toks)
         d_kpr = torch.empty_like(kpr)
+        cs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        nrot = max(2, arm.n_rot)
+        tgt = target if len(target) >= 2 else target * 2
+        drf = draft if len(draft) >= 2 else draft * 2
+        ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(nrot)]
+
+        def halves(t):
+            flat = t.view(-1)
+            n = flat.numel() // 2
+            return (flat[:n], flat[n:])
 
         def e2e_step(i):
-            c = i % ROTATE
-            target[c].copy_(h_target, non_blocking=True)
-            draft[c].copy_(h_draft, non_blocking=True)
-            d_toks.copy_(h_toks, non_blocking=True)
-            d_kpr.copy_(h_kpr, non_blocking=True)
-            o = ver.run(target[c], draft[c], d_toks, d_kpr, out=out, debug=False,
-                        w_vocab=wv if fused else None, **knobs)
+            c = i % nrot
+            # the copies into buffer c wait for the step that last read it
+            for k, (dst, src) in enumerate(((tgt[c], h_target), (drf[c], h_draft))):
+                s = cs[k]
+                s.wait_event(done[c])
+                with torch.cuda.stream(s):
+                    dst.copy_(src, non_blocking=True)
+                    if k == 0:
+                        d_toks.copy_(h_toks, non_blocking=True)
+                        d_kpr.copy_(h_kpr, non_blocking=True)
+                ready[k].record(s)
+            stream.wait_event(ready[0])
+            stream.wait_event(ready[1])
+            o = arm.ver.run(tgt[c], drf[c], d_toks, d_kpr, out=out, debug=False,
+                            w_vocab=arm.wv, **arm.knobs)
+            done[c].record(stream)
             h_out_t.copy_(o["tokens"], non_blocking=True)
             h_out_n.copy_(o["num_accepted"], non_blocking=True)
 
@@ -506,6 +635,8 @@ def run_gpu(args):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
+        for s in cs:
+            s.wait_event(a)
         for i in range(args.e2e_steps):
             e2e_step(i)
         b.record(stream)
@@ -516,7 +647,25 @@ def run_gpu(args):
         d2h = h_out_t.numel() * 4 + h_out_n.numel() * 4
         e2e = {"value": whole_job_rate(rows, args.e2e_steps, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
+               "copies": "target and draft on two copy streams, double-buffered"}
+
+    fused = arm.fused
+    verify_stage = _verify_stage(arm, 1e3 * mean_step_ms, ks["median_us"], peak) if fused else {}
+    toks_np = arm.toks.cpu().numpy()
+    draft0 = arm.draft[0].cpu().numpy() if fused else None
+    l2_note = arm.l2
+    arm.close()
+    del arm
+    torch.cuda.empty_cache()
+
+    others = None
+    if rank == 0 and world == 1 and not args.no_others and not args.batch and not args.early_exit:
+        others = {}
+        for n in (1, 2, 3, 4, 5):
+            if n == args.config:
+                continue
+            others[str(n)] = workload_summary(sv, torch, n, dev, local, K, args.warmup, peak)
 
     if rank != 0:
         if dist:
@@ -525,12 +674,12 @@ def run_gpu(args):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         if fused:
-            cpu = cpu_baseline_fused(w, draft[0].cpu().numpy(), toks.cpu().numpy(),
-                                     seconds_target=args.cpu_seconds)
+            cpu = cpu_baseline_fused(w, draft0, toks_np, seconds_target=args.cpu_seconds)
         else:
-            cpu = cpu_baseline(w, toks.cpu().numpy(), seconds_target=args.cpu_seconds)
+            cpu = cpu_baseline(w, toks_np, seconds_target=args.cpu_seconds)
     cfg = _wl_config(w, ROTATE)
     cfg["config_id"] = args.config
+    cfg["l2"] = l2_note
     if args.batch:
         cfg["workload"] += f" (B overridden to {w.B})"
     if args.early_exit:
@@ -539,7 +688,9 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (arithmetic; inputs " + ("bf16 hidden/W" if fused else w.dtype) + ")",
+        "data": "synthetic",
         "config": cfg,
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -547,33 +698,25 @@ def run_gpu(args):
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "traffic": _traffic(kernel, w),
                      "algorithmic_bytes_per_launch": bytes_step,
-                     "mean_launch_us": mean_kern_ms * 1e3,
-                     "launches_timed": len(kern_ms),
+                     "launch_us": ks,
+                     "launches_timed": ks["n"],
                      "step_us": mean_step_ms * 1e3,
-                     "step_frac": bytes_step / (mean_step_ms / 1e3) / 1e9 / peak},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                     "step_frac": bytes_step / (mean_step_ms / 1e3) / 1e9 / peak,
+                     "host_enqueue_us_per_step": r["host_us_per_step"]},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": r["launches"],
         "clocks": clocks,
     }
-    if fused:
-        # the verify stage of the fused round: the step without the LM head,
-        # against the bytes of its rows (target logits + draft probabilities)
-        vb = w.logit_bytes()
-        v_us = (mean_step_ms - mean_kern_ms) * 1e3
-        line["verify_stage"] = {"us": v_us, "algorithmic_bytes": vb,
-                                "achieved_gbs": vb / (v_us * 1e-6) / 1e9,
-                                "frac": vb / (v_us * 1e-6) / 1e9 / peak,
-                                "note": "mean step time minus the LM head's live time; the kernels "
-                                        "read the draft probabilities only at drafted tokens "
-                                        "and at the resampled row"}
+    line.update(verify_stage)
     if flops:
         tf = _tensor_peak()
         line["roofline"]["tensor"] = {
-            "achieved_tflops": flops / (mean_kern_ms / 1e3) / 1e12, "peak_tflops": tf,
-            "frac": flops / (mean_kern_ms / 1e3) / 1e12 / tf if tf else None,
+            "achieved_tflops": flops / (ks["median_us"] * 1e-6) / 1e12, "peak_tflops": tf,
+            "frac": flops / (ks["median_us"] * 1e-6) / 1e12 / tf if tf else None,
             "flops_per_launch": flops,
             "peak_source": "measured bf16_tflops (MEASURED_PEAKS.json), burst"}
+    if others is not None:
+        line["workloads"] = others
     print(json.dumps(line), flush=True)
-    ver.close()
     if dist:
         dist.destroy_process_group()
 
@@ -593,6 +736,8 @@ def main(argv=None):
     ap.add_argument("--early-exit", action="store_true",
                     help="time spec_verify_run_early_exit (top-k rows of logits)")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's B")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-workload summaries of the other four workloads")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="reference arm: stop the timed loop after this much oracle time")
     args = ap.parse_args(argv)

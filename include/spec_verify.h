@@ -73,7 +73,7 @@ typedef enum {
     SPEC_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement        */
     SPEC_ERR_OOM = 3,         /* workspace allocation failed (create only)              */
     SPEC_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed            */
-    SPEC_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait ran out           */
+    SPEC_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (spec_verify_check) */
 } spec_status;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -210,10 +210,17 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
  * used: the sizes come from `in`).
  *  - The first call on a device looks up the array's device address on that
  *    device (once); make that first call before any stream capture begins.
+ *  - A configuration with the fused LM head (SPEC_TARGET_HIDDEN_LMHEAD)
+ *    returns SPEC_ERR_UNSUPPORTED: its fp32 logits alone exceed the array.
  *  - Sizes whose workspace would not fit the array return
- *    SPEC_ERR_INVALID_ARG and launch nothing.  At V = 128256 and bf16 about
- *    1100 row slots fit (B * (2 K_max + 1), e.g. B = 64 with K_max = 8); the
- *    workspace per row slot is about 12.5 KB plus 4 bytes per 64 tokens.
+ *    SPEC_ERR_INVALID_ARG and launch nothing.  The workspace is about
+ *      per row slot (B * (2 K_max + 1) of them): 8244 bytes + 16 bytes per
+ *        segment of 16 KB of the row + 2 bytes per 128-byte chunk of the row,
+ *        i.e. 12.2 KiB at V = 128256 bf16 and 16.4 KiB at V = 128256 fp32;
+ *      per drafted slot (B * K_max of them): 28 bytes + 40 bytes per 4096
+ *        tokens, i.e. 1.28 KiB at V = 128256;
+ *    so B = 64 with K_max = 8 at V = 128256 bf16 (1088 row slots, 512
+ *    drafted slots) needs 14.3 MB.
  *  - Every call shares the one array and each call reuses the last call's
  *    contents (the counters that must start at zero are cleared on the
  *    stream first), so calls that overlap on the GPU race: issue them on one
@@ -249,6 +256,45 @@ spec_status spec_lmhead_logits(const void* hidden, const void* w_vocab, int32_t 
  * a run with the hook set can take slightly longer. */
 spec_status spec_verify_set_profiling(spec_verify_t h, void* ev_stage1_begin, void* ev_stage1_end,
                                       int32_t* launches_out);
+
+/* Device-side failure report (the pages have no counterpart).  Every wait
+ * of the library's kernels on a copy or on another warp is bounded; a wait
+ * that runs out records it in the handle's workspace and its kernel returns
+ * early, which leaves that run's outputs undefined but the CUDA context
+ * usable.  This call waits for the work queued on `stream` (a cudaStream_t
+ * as void*, NULL the legacy default stream), reads the record and clears it.
+ * Returns SPEC_ERR_TIMEOUT when a run of the handle since the last check ran
+ * out of a wait, SPEC_OK when none did, SPEC_ERR_INVALID_ARG for a NULL
+ * handle and SPEC_ERR_CUDA when the wait or the read fails. */
+spec_status spec_verify_check(spec_verify_t h, void* stream);
+
+/* Fault injection for tests of the failure report (the pages have no
+ * counterpart); it acts on the host side only.  SPEC_FAULT_STALL_STREAM makes
+ * the next spec_verify_run of the handle launch only its stage-1 stream
+ * kernel, whose producer issues no copy, so that the consumers' waits run out
+ * after a short limit (4096 polls) and record a timeout; no other kernel of
+ * that run is launched and its outputs are not written.  It applies to one
+ * run, then resets to SPEC_FAULT_NONE.  The run returns
+ * SPEC_ERR_UNSUPPORTED (and the fault stays armed) when its rows do not take
+ * the stream kernel (rows not on 16 bytes, the LM head).  Returns
+ * SPEC_ERR_INVALID_ARG for a NULL handle or an unknown fault. */
+enum { SPEC_FAULT_NONE = 0, SPEC_FAULT_STALL_STREAM = 1 };
+spec_status spec_verify_inject_fault(spec_verify_t h, int32_t fault);
+
+/* Workspace allocator (the pages have no counterpart).  By default a handle's
+ * workspace comes from cudaMalloc and goes back with cudaFree.  A caller that
+ * manages device memory itself (a pooled allocator, a memory budget) installs
+ * alloc / release here: spec_verify_create then calls alloc(ctx, bytes,
+ * device, &ptr) with `device` current, which returns 0 and a device pointer
+ * aligned to 256 bytes on success and nonzero on failure (create then returns
+ * SPEC_ERR_OOM); spec_verify_destroy calls release(ctx, ptr, device).  A
+ * handle keeps the functions it was created with.  Passing NULL for both
+ * restores cudaMalloc / cudaFree.  The setting is process-wide and applies to
+ * handles created after the call.  Returns SPEC_ERR_INVALID_ARG when exactly
+ * one of the two functions is NULL. */
+typedef int (*spec_alloc_fn)(void* ctx, uint64_t bytes, int32_t device, void** ptr);
+typedef void (*spec_release_fn)(void* ctx, void* ptr, int32_t device);
+spec_status spec_verify_set_allocator(spec_alloc_fn alloc, spec_release_fn release, void* ctx);
 
 /* Free the handle and its workspace (synchronises its device first). */
 spec_status spec_verify_destroy(spec_verify_t h);

@@ -28,7 +28,13 @@ SPEC_ROW_OK, SPEC_ROW_BAD_TOKEN, SPEC_ROW_BAD_K, SPEC_ROW_NONFINITE, \
 # every function the header declares (checked by the tests)
 ABI_FUNCTIONS = ("spec_verify_create", "spec_verify_run", "spec_draft_sample",
                  "spec_verify_destroy", "spec_verify_status_string", "spec_verify_run_noalloc",
-                 "spec_verify_set_profiling", "spec_lmhead_logits", "spec_verify_run_early_exit")
+                 "spec_verify_set_profiling", "spec_lmhead_logits", "spec_verify_run_early_exit",
+                 "spec_verify_check", "spec_verify_inject_fault", "spec_verify_set_allocator")
+SPEC_FAULT_NONE, SPEC_FAULT_STALL_STREAM = 0, 1
+
+# spec_alloc_fn / spec_release_fn of spec_verify_set_allocator
+SPEC_ALLOC_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_uint64, C.c_int32, C.POINTER(C.c_void_p))
+SPEC_RELEASE_FN = C.CFUNCTYPE(None, C.c_void_p, C.c_void_p, C.c_int32)
 SPEC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -100,6 +106,12 @@ def load_library(path: str | None = None) -> C.CDLL:
     L.spec_lmhead_logits.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
                                      C.c_void_p, C.c_void_p]
     L.spec_lmhead_logits.restype = C.c_int
+    L.spec_verify_check.argtypes = [C.c_void_p, C.c_void_p]
+    L.spec_verify_check.restype = C.c_int
+    L.spec_verify_inject_fault.argtypes = [C.c_void_p, C.c_int32]
+    L.spec_verify_inject_fault.restype = C.c_int
+    L.spec_verify_set_allocator.argtypes = [SPEC_ALLOC_FN, SPEC_RELEASE_FN, C.c_void_p]
+    L.spec_verify_set_allocator.restype = C.c_int
     if path is None:
         _lib = L
     return L
@@ -174,6 +186,29 @@ def spec_lmhead_logits(hidden: int, w_vocab: int, m: int, hidden_dim: int, vocab
                                              int(hidden_dim), int(vocab), C.c_void_p(logits),
                                              C.c_void_p(stream)),
            "spec_lmhead_logits")
+
+
+def spec_verify_check(h, stream: int = 0) -> int:
+    """Wait for `stream`, then read and clear the handle's device-side failure
+    record: SPEC_OK, or SPEC_ERR_TIMEOUT when a bounded wait of a run ran out
+    (returned, not raised; other errors raise)."""
+    code = load_library().spec_verify_check(h, C.c_void_p(stream))
+    if code not in (SPEC_OK, SPEC_ERR_TIMEOUT):
+        _check(code, "spec_verify_check")
+    return code
+
+
+def spec_verify_inject_fault(h, fault: int) -> None:
+    _check(load_library().spec_verify_inject_fault(h, int(fault)), "spec_verify_inject_fault")
+
+
+def spec_verify_set_allocator(alloc, release, ctx: int | None = None) -> None:
+    """alloc / release: SPEC_ALLOC_FN / SPEC_RELEASE_FN objects (keep them
+    alive while handles created with them exist), or None for both."""
+    _check(load_library().spec_verify_set_allocator(alloc or SPEC_ALLOC_FN(),
+                                                    release or SPEC_RELEASE_FN(),
+                                                    C.c_void_p(ctx or 0)),
+           "spec_verify_set_allocator")
 
 
 def spec_verify_destroy(h) -> None:

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "sv_internal.cuh"
@@ -42,6 +43,14 @@ struct spec_verify {
     cudaEvent_t prof_end;
     int32_t* prof_launches;
     float* logits;        // the LM head's output (SPEC_TARGET_HIDDEN_LMHEAD), else NULL
+    int fault;            // spec_verify_inject_fault: the fault armed for the next run
+    // chunk keys may be left nonzero by a launch other than the fused top-k
+    // kernel (which needs them at 0 when it starts): clear them before it
+    bool keys_dirty;
+    // where the workspace came from (NULL: cudaMalloc / cudaFree)
+    spec_alloc_fn alloc_fn;
+    spec_release_fn release_fn;
+    void* alloc_ctx;
 };
 
 namespace {
@@ -67,6 +76,22 @@ struct DeviceGuard {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// spec_verify_set_allocator: the functions later handles take their workspace from
+struct AllocHook {
+    std::mutex mu;
+    spec_alloc_fn alloc = nullptr;
+    spec_release_fn release = nullptr;
+    void* ctx = nullptr;
+};
+AllocHook& alloc_hook()
+{
+    static AllocHook hook;
+    return hook;
+}
+
+// polls of a wait that runs out on purpose (SPEC_FAULT_STALL_STREAM)
+constexpr uint32_t STALL_WAIT_POLLS = 4096;
+
 // knobs of one launch; SPEC_OK or the error to return
 spec_status fill_knobs(const spec_verify* h, const spec_sampling* s, Params& p)
 {
@@ -82,6 +107,7 @@ spec_status fill_knobs(const spec_verify* h, const spec_sampling* s, Params& p)
     p.greedy = T == 0.f ? 1 : 0;
     p.T = p.greedy ? 1.f : T;
     p.c = (float)(1.4426950408889634 / (double)p.T);
+    p.c_lo = (float)(1.4426950408889634 / (double)p.T - (double)p.c);
     p.top_k = p.greedy ? (V > 1 ? 1 : 0) : (s->top_k > 0 && s->top_k < V) ? s->top_k : 0;
     p.top_p = p.greedy ? 1.f : s->top_p < 1.f ? s->top_p : 1.f;
     p.top_p_fix = !p.greedy && s->top_p < 1.f ? (uint64_t)((double)s->top_p * 72057594037927936.0) : 0;
@@ -128,7 +154,10 @@ size_t layout_workspace(spec_verify* h, void* base)
     if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD)
         h->nseg_cap = (int)std::max<int64_t>(h->nseg_cap, cdiv(V, LM_STAT_COLS));
     h->nseg_sample = (int)cdiv(V, SAMPLE_SEG);
-    h->chunk_stride = (int)(cdiv(h->nchunk_cap, 8) * 8);
+    // the chunk-key area of a row slot also holds its key histograms (bf16
+    // rows with top-p alone): HIST_BINS bytes per 16 KB segment
+    const int64_t hist_keys = cdiv(V, seg_elems(SPEC_BF16)) * HIST_BINS / 2;
+    h->chunk_stride = (int)(cdiv(std::max<int64_t>(h->nchunk_cap, hist_keys), 8) * 8);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -177,11 +206,28 @@ size_t layout_workspace(spec_verify* h, void* base)
 // stage 1: stream every row (the persistent bulk-copy kernel when every row
 // starts on a 16-byte boundary, else one CTA per segment); then merge the rows
 // (one warp per row when the knobs allow, else one CTA per row) and decide the
-// sequences, each grid a programmatic dependent launch of the one before
-cudaError_t launch_stage1(const spec_verify* h, const Params& p, int dtype, bool vec,
-                          cudaStream_t s, int* launches, bool timed = true)
+// sequences, each grid a programmatic dependent launch of the one before.
+// Top-k rows on 16 bytes take the fused kernel instead (stream and row merges
+// in one grid), then the decision grid.
+cudaError_t launch_stage1(spec_verify* h, Params& p, int dtype, bool vec, cudaStream_t s, int* launches,
+                          bool timed = true, bool allow_fused = true)
 {
     const bool rec = timed && h->prof_begin;
+    if (allow_fused && p.cand && vec) {
+        if (h->keys_dirty) {
+            const size_t kb = sizeof(uint16_t) * (size_t)h->chunk_stride * (size_t)p.B * (size_t)p.rps;
+            if (cudaMemsetAsync(h->chunk, 0, kb, s) != cudaSuccess) return cudaErrorUnknown;
+            h->keys_dirty = false;
+        }
+        p.fused = 1;
+        if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
+        cudaError_t e = launch_verify_topk(p, dtype, h->num_sms, s);
+        if (e != cudaSuccess) return e;
+        if (rec && cudaEventRecord(h->prof_end, s) != cudaSuccess) return cudaErrorUnknown;
+        *launches += 2;
+        return launch_decide(p, dtype, s);
+    }
+    if (p.seg_mode != SEG_SUM) h->keys_dirty = true;  // chunk keys or key histograms
     if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
     cudaError_t e = vec ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
                         : launch_rows(p, dtype, false, s);
@@ -204,6 +250,15 @@ void choose_seg_mode(Params& p, int dtype)
     const bool fast = p.top_k > 0 && p.top_k <= KCAP && p.top_k <= p.nchunk &&
                       p.nchunk <= MAX_CHUNKS;
     p.seg_mode = fast ? SEG_CHUNK : SEG_SUM;
+}
+
+// bf16 rows with top-p alone, streamed by the bulk-copy kernel: per-segment
+// key histograms, from which the row merge cuts the nucleus without reading
+// the row again
+void use_key_histograms(Params& p, int dtype, bool vec)
+{
+    if (vec && dtype == SPEC_BF16 && p.seg_mode == SEG_SUM && p.top_k == 0 && p.top_p < 1.f && !p.greedy)
+        p.seg_mode = SEG_HIST;
 }
 
 }  // namespace
@@ -271,14 +326,32 @@ spec_status spec_verify_create(const spec_verify_config* cfg, spec_verify_t* out
         return SPEC_ERR_INVALID_ARG;
     }
     h->ws_bytes = layout_workspace(h, nullptr);
+    {
+        AllocHook& hook = alloc_hook();
+        std::lock_guard<std::mutex> lock(hook.mu);
+        h->alloc_fn = hook.alloc;
+        h->release_fn = hook.release;
+        h->alloc_ctx = hook.ctx;
+    }
     void* base = nullptr;
-    if (cudaMalloc(&base, h->ws_bytes) != cudaSuccess) {
+    if (h->alloc_fn) {
+        if (h->alloc_fn(h->alloc_ctx, (uint64_t)h->ws_bytes, cfg->device, &base) != 0 || !base) {
+            delete h;
+            return SPEC_ERR_OOM;
+        }
+        if ((uintptr_t)base & 255u) {  // the sub-buffers need 256-byte alignment
+            h->release_fn(h->alloc_ctx, base, cfg->device);
+            delete h;
+            return SPEC_ERR_INVALID_ARG;
+        }
+    } else if (cudaMalloc(&base, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return SPEC_ERR_OOM;
     }
     if (cudaMemset(base, 0, h->ws_bytes) != cudaSuccess) {
-        cudaFree(base);
+        if (h->alloc_fn) h->release_fn(h->alloc_ctx, base, cfg->device);
+        else cudaFree(base);
         delete h;
         return SPEC_ERR_CUDA;
     }
@@ -333,6 +406,7 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
     choose_seg_mode(p, dtype);
     const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(p.target) &&
                      (cfg.draft_kind == SPEC_DRAFT_PROBS || aligned16(in->draft));
+    use_key_histograms(p, dtype, vec);
     // top-k rows: the chunks reaching the row's bound gathered by one CTA per row
     p.cand = vec && p.seg_mode == SEG_CHUNK && warp_merge_ok(p) && p.top_k >= 1 &&
              p.top_k <= CAND_TOPK_MAX;
@@ -341,6 +415,18 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
     if (!g.ok) return SPEC_ERR_CUDA;
     cudaStream_t cs = (cudaStream_t)stream;
     int launches = 0;
+    if (h->fault == SPEC_FAULT_STALL_STREAM) {
+        // the stream kernel alone, its producer idle: the consumers' waits run out
+        if (!vec || lmhead) return SPEC_ERR_UNSUPPORTED;
+        h->fault = SPEC_FAULT_NONE;
+        p.stall = 1;
+        p.wait_limit = STALL_WAIT_POLLS;
+        if (p.seg_mode != SEG_SUM) h->keys_dirty = true;
+        if (launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, cs) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        if (h->prof_launches) *h->prof_launches = 1;
+        return SPEC_OK;
+    }
     // rows without top-k / top-p after the LM head: its epilogue writes the
     // softmax partials per 256-column tile and no stream pass is needed
     const bool lm_stats = lmhead && p.seg_mode == SEG_SUM && warp_merge_ok(p);
@@ -363,6 +449,7 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
     // it returns at once unless that kernel raised the flag
     const bool exit = early_exit && p.cand && !lmhead;
     if (exit) {
+        h->keys_dirty = true;  // the early-exit kernel writes chunk keys
         p.exit_flag = h->exit_flag;
         if (cudaMemsetAsync(h->exit_flag, 0, sizeof(unsigned), cs) != cudaSuccess) return SPEC_ERR_CUDA;
         if (h->prof_begin && cudaEventRecord(h->prof_begin, cs) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -374,7 +461,7 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
         // the row merge (softmax partials of the LM head) and the decision grid
         launches += 2;
         if (launch_merge_warp(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
-    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead && !exit) != cudaSuccess) {
+    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead && !exit, !exit) != cudaSuccess) {
         return SPEC_ERR_CUDA;
     }
     if (!all_lists(p)) {
@@ -433,6 +520,7 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
     const int dtype = cfg.draft_dtype;
     choose_seg_mode(p, dtype);
     const bool vec = ((int64_t)p.V * elem_size(dtype)) % 16 == 0 && aligned16(draft);
+    use_key_histograms(p, dtype, vec);
 
     DeviceGuard g(cfg.device);
     if (!g.ok) return SPEC_ERR_CUDA;
@@ -468,6 +556,51 @@ spec_status spec_verify_set_profiling(spec_verify_t h, void* ev_stage1_begin, vo
     return SPEC_OK;
 }
 
+spec_status spec_verify_check(spec_verify_t h, void* stream)
+{
+    if (!h) return SPEC_ERR_INVALID_ARG;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return SPEC_ERR_CUDA;
+    cudaStream_t cs = (cudaStream_t)stream;
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, h->err, sizeof word, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    if (word == 0) return SPEC_OK;
+    // a run that gave up may leave tickets and chunk keys behind: clear them
+    if (cudaMemsetAsync(h->err, 0, sizeof(unsigned), cs) != cudaSuccess ||
+        cudaMemsetAsync(h->row_ticket, 0, sizeof(unsigned) * (size_t)h->rows_cap, cs) != cudaSuccess ||
+        cudaMemsetAsync(h->seq_ticket, 0, sizeof(unsigned) * (size_t)h->cfg.max_batch, cs) != cudaSuccess ||
+        cudaMemsetAsync(h->seq_done, 0, sizeof(unsigned) * (size_t)h->cfg.max_batch, cs) != cudaSuccess ||
+        cudaMemsetAsync(h->job_ticket, 0, sizeof(unsigned) * (size_t)h->jobs_cap, cs) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    h->keys_dirty = true;
+    return SPEC_ERR_TIMEOUT;
+}
+
+spec_status spec_verify_inject_fault(spec_verify_t h, int32_t fault)
+{
+    if (!h || (fault != SPEC_FAULT_NONE && fault != SPEC_FAULT_STALL_STREAM)) return SPEC_ERR_INVALID_ARG;
+    h->fault = fault;
+    return SPEC_OK;
+}
+
+spec_status spec_verify_set_allocator(spec_alloc_fn alloc, spec_release_fn release, void* ctx)
+{
+    if ((!alloc) != (!release)) return SPEC_ERR_INVALID_ARG;
+    AllocHook& hook = alloc_hook();
+    std::lock_guard<std::mutex> lock(hook.mu);
+    hook.alloc = alloc;
+    hook.release = release;
+    hook.ctx = alloc ? ctx : nullptr;
+    return SPEC_OK;
+}
+
 spec_status spec_verify_destroy(spec_verify_t h)
 {
     if (!h) return SPEC_ERR_INVALID_ARG;
@@ -475,7 +608,12 @@ spec_status spec_verify_destroy(spec_verify_t h)
     {
         DeviceGuard g(h->cfg.device);
         if (!g.ok) st = SPEC_ERR_CUDA;
-        if (h->ws && cudaFree(h->ws) != cudaSuccess) st = SPEC_ERR_CUDA;
+        if (h->ws && h->release_fn) {
+            if (cudaDeviceSynchronize() != cudaSuccess) st = SPEC_ERR_CUDA;
+            h->release_fn(h->alloc_ctx, h->ws, h->cfg.device);
+        } else if (h->ws && cudaFree(h->ws) != cudaSuccess) {
+            st = SPEC_ERR_CUDA;
+        }
     }
     delete h;
     return st;
@@ -535,6 +673,7 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
     const size_t need = layout_over(&h, cfg, in->batch, in->k_max, ws, ws_bytes);
     if (need == 0 || need > ws_bytes) return SPEC_ERR_INVALID_ARG;
     h.num_sms = num_sms;
+    h.keys_dirty = true;  // the array keeps whatever the last call left in its chunk keys
     // the counters the kernels expect at zero (the array keeps the last call's contents)
     cudaStream_t cs = (cudaStream_t)stream;
     const size_t tickets = sizeof(unsigned) * (size_t)h.rows_cap;

@@ -299,13 +299,11 @@ __global__ void __launch_bounds__(STREAM_THREADS, EXIT_CTAS_PER_SM) k_verify_exi
 template <typename T>
 static cudaError_t launch_verify_exit_t(const Params& p, int num_sms, cudaStream_t s)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_verify_exit<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             STREAM_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static DeviceOnce once;  // the shared-memory opt-in, per device
+    const cudaError_t e = cuda_once(once, nullptr, [](int, int*) {
+        return cudaFuncSetAttribute(k_verify_exit<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+    });
+    if (e != cudaSuccess) return e;
     const int grid = std::min(p.B, EXIT_CTAS_PER_SM * num_sms);
     if (grid <= 0) return cudaSuccess;
     k_verify_exit<T><<<grid, STREAM_THREADS, STREAM_SMEM, s>>>(p);

@@ -21,7 +21,19 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "sv_once.h"
+
 namespace sv {
+
+// the current device's one-time launch set-up (sv_once.h)
+template <typename F>
+inline cudaError_t cuda_once(DeviceOnce& o, int* value, F setup)
+{
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return device_once(o, dev, cudaSuccess, cudaErrorInvalidDevice, value, setup);
+}
 
 constexpr int NT = 256;             // threads of every CTA
 constexpr int SEG_BYTES = 16384;    // bytes of one stage-1 segment
@@ -42,7 +54,12 @@ constexpr int NS = 128;             // stream threads of the streaming kernel
 constexpr int STREAM_THREADS = NS + 32;
 constexpr int STREAM_CTAS_PER_SM = 3;
 
-enum SegMode : int32_t { SEG_SUM = 0, SEG_CHUNK = 1 };
+// SEG_SUM: per-segment (max, sum exp); SEG_CHUNK: 16-bit chunk-max keys;
+// SEG_HIST (bf16 rows with top-p alone): per-segment max, a count of tokens at
+// each of the HIST_BINS order keys from the max down, and the sum of exp over
+// the tokens below them
+enum SegMode : int32_t { SEG_SUM = 0, SEG_CHUNK = 1, SEG_HIST = 2 };
+constexpr int HIST_BINS = 256;      // bf16 keys counted below a segment's max (two binades)
 enum RowMode : int32_t { MODE_ALL = 0, MODE_LIST = 1, MODE_PREFIX = 2 };
 enum : int32_t { FLAG_NONFINITE = 1, FLAG_BLOCK_MERGE = 2 };  // 2: the warp merge gave up
 enum : int32_t { JOB_NONE = 0, JOB_RESIDUAL = 1, JOB_ROW = 2 };
@@ -93,6 +110,7 @@ struct Params {
     // knobs
     float T;              // temperature
     float c;              // log2(e) / T (fp32, used by every exponential)
+    float c_lo;           // log2(e) / T - c (fp32): c + c_lo carries the ratio to ~2^-48
     int32_t top_k;        // 0: off
     float top_p;          // >= 1: off
     uint64_t top_p_fix;   // top_p in units of 2^-56
@@ -129,6 +147,15 @@ struct Params {
     int32_t cand;             // 1: top-k rows (1 <= top-k <= CAND_TOPK_MAX) take k_merge_cand
     unsigned* exit_flag;      // early exit: the regular pipeline runs only when it is nonzero (NULL: always)
     unsigned* seq_done;       // [B] sequences decided inside the merge grid
+    // fault injection (tests of the timeout report): the stream kernel's
+    // producer issues no copy and its consumers' waits give up after
+    // wait_limit polls; 0 / 0 in every ordinary run
+    int32_t stall;
+    uint32_t wait_limit;      // 0: WAIT_LIMIT
+    // 1: the top-k rows run the fused kernel (sv_fused.cuh), which takes a 0
+    // chunk key for a chunk not streamed yet; whoever reads a row's keys last
+    // writes 0 back
+    int32_t fused;
 };
 
 constexpr int CAND_TOPK_MAX = 128;  // largest top-k the row merge of sv_mcand.cuh serves
@@ -161,6 +188,18 @@ __device__ __forceinline__ float ex2_fast(float x)
     float r;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
+}
+
+// order key of a bf16 bit pattern (16 bits; -0 folded onto +0), and back
+__device__ __forceinline__ uint32_t key16_bf16(uint32_t b)
+{
+    if (b == 0x8000u) b = 0u;
+    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+__device__ __forceinline__ float val_key16(uint32_t k)
+{
+    const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(b << 16);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -259,6 +298,16 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(N
 
 // barrier of the stream warps of the streaming kernel (named barrier 2)
 __device__ __forceinline__ void ssync() { asm volatile("bar.sync 2, %0;" ::"n"(NS) : "memory"); }
+// the same barrier, returning whether v held in every stream thread (so that
+// a bounded wait that ran out in one thread ends the loop in all of them)
+__device__ __forceinline__ bool ssync_and(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+                 "bar.red.and.pred p, 2, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)v), "n"(NS) : "memory");
+    return r != 0;
+}
 
 // reductions over a thread group of NTH threads (local index lt) whose
 // barrier is SYNC(); red holds NTH/32 values
@@ -532,6 +581,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// the same with a limit of `limit` polls (0: WAIT_LIMIT)
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint32_t limit)
+{
+    const uint32_t n = limit ? limit : WAIT_LIMIT;
+    for (uint32_t i = 0; i < n; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
 // one-dimensional bulk copy global -> shared, completing on an mbarrier
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
 {
@@ -561,6 +618,10 @@ cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_
 // top-k rows: the row merge (one CTA per row) and the decision grid for what
 // it leaves, both programmatic dependents of the stream
 cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s);
+// top-k rows as one persistent kernel (stream and row merges at once,
+// cooperative launch), then the decision grid for what it leaves
+cudaError_t launch_verify_topk(const Params& p, int dtype, int num_sms, cudaStream_t s);
+cudaError_t launch_decide(const Params& p, int dtype, cudaStream_t s);
 // early-exit verify of the top-k rows (one CTA per sequence at a time)
 cudaError_t launch_verify_exit(const Params& p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);

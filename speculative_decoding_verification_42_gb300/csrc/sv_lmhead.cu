@@ -7,20 +7,22 @@
 // Sampling", The cost of one token, is the target model's forward pass that
 // produces these logits).
 //
-// Persistent clusters of two CTAs on neighbouring 128-row blocks of H share
-// each 64-deep K slice of W: every CTA copies half of the slice's 256 columns
-// and multicasts it to both (W crosses HBM once), and its own 128 rows of H.
-// Per CTA, lane 0 of warp 0 fills a four-stage shared-memory ring with
-// tensor-map bulk copies (128-byte swizzle); lane 0 of warp 1 issues
-// tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M = 128, N = 256, K = 16) into
-// one of two tensor-memory accumulators and frees each stage in both CTAs
-// with a multicast tcgen05.commit; warps 2..5 read the other accumulator back
-// (tcgen05.ld, one row per thread) and store the fp32 tile meanwhile.  H is
-// the K-major A operand; W, whose rows run along the vocabulary, is the
-// N-major B operand.  On request the epilogue also writes, per row and
-// 256-column tile, the softmax partials (max, sum exp2((l - max) c)) that
-// the verify's row merge combines, so that no pass over the logits is needed
-// for rows without top-k / top-p.
+// Persistent pairs of CTAs (clusters of two) each own a 256 x 256 output tile
+// per turn and issue one 2-SM MMA (tcgen05.mma.cta_group::2, M = 256, N =
+// 256, K = 16): CTA r of the pair holds rows 128 r .. 128 r + 127 of the
+// tile's H block (the A operand, K-major) and columns 128 r .. 128 r + 127 of
+// the tile's W slice (the B operand, N-major) in its own shared memory, and
+// its tensor memory receives its 128 rows x all 256 columns of the product.
+// Every byte of W crosses HBM once and each CTA copies only its own half:
+// lane 0 of warp 0 of each CTA fills a six-stage ring with tensor-map copies
+// (128-byte swizzle) whose completion is counted on the even CTA's barrier;
+// lane 0 of warp 1 of the even CTA issues the MMAs into one of two
+// accumulators and commits each stage's release to both CTAs' barriers;
+// warps 2..5 of each CTA read the other accumulator back (tcgen05.ld, one row
+// per thread) and store the fp32 tile meanwhile.  On request the epilogue
+// also writes, per row and 256-column tile, the softmax partials (max, sum
+// exp2((l - max) c)) that the verify's row merge combines, so that no pass
+// over the logits is needed for rows without top-k / top-p.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
 
 #include <algorithm>
@@ -30,41 +32,46 @@
 
 namespace sv {
 
-constexpr int LM_BM = 128, LM_BN = 256, LM_BK = 64, LM_STAGES = 4;
+constexpr int LM_BM = 128, LM_BN = 256, LM_BK = 64, LM_STAGES = 6;
+constexpr int LM_BNH = LM_BN / 2;                  // W columns held by one CTA of the pair
 constexpr int LM_A_BYTES = LM_BM * LM_BK * 2;      // 16 KB: 128 rows of one 128-byte swizzle row
-constexpr int LM_B_BYTES = LM_BK * LM_BN * 2;      // 32 KB: four 64-column boxes of 64 K-rows
 constexpr int LM_BOX_B = LM_BK * 64 * 2;           // 8 KB: one W box (64 K-rows x 64 columns)
+constexpr int LM_B_BYTES = LM_BK * LM_BNH * 2;     // 16 KB: two W boxes
 constexpr int LM_STAGE_BYTES = LM_A_BYTES + LM_B_BYTES;
 constexpr int LM_SMEM = LM_STAGES * LM_STAGE_BYTES + 1024;  // + slack for 1024-byte alignment
 constexpr int LM_THREADS = 192;                     // producer, MMA, four epilogue warps
 constexpr uint32_t LM_ACC_COLS = 256;               // fp32 accumulator: 128 lanes x 256 columns
 constexpr uint32_t LM_TMEM_COLS = 2 * LM_ACC_COLS;  // two accumulators
-static_assert(LM_BN == 4 * 64, "each CTA of the pair copies two 64-column boxes of W");
+static_assert(LM_BNH == 2 * 64, "each CTA of the pair copies two 64-column boxes of W");
 static_assert(LM_BN == LM_STAT_COLS, "the softmax partials are per column tile");
+static_assert(LM_SMEM <= 227 * 1024, "the ring fits one CTA's shared memory");
 
 // ------------------------------------------------------------------------- //
 // PTX wrappers                                                              //
 // ------------------------------------------------------------------------- //
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar)
+// the shared::cluster address of the same shared-memory location in CTA `rank`
+__device__ __forceinline__ uint32_t lm_mapa(const void* p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// a tensor-map box into this CTA's shared memory; its bytes count on the
+// mbarrier at cluster address bar (either CTA of the pair)
+__device__ __forceinline__ void lm_tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                          uint64_t pol)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
         : "memory");
 }
-
-// the same box into the same shared-memory offset of every CTA in cta_mask,
-// completing on the mbarrier at the same offset in each
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t cta_mask)
+__device__ __forceinline__ uint64_t l2_evict_last()
 {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // shared-memory matrix descriptor, 128-byte swizzle: start address, leading
@@ -76,28 +83,28 @@ __device__ __forceinline__ uint64_t lm_sdesc(uint32_t saddr, uint32_t lbo, uint3
 }
 
 // instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A
-// K-major, B N-major, M = 128, N = 256
+// K-major, B N-major, M = 256 (the pair), N = 256
 constexpr uint32_t LM_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                              ((uint32_t)(LM_BN >> 3) << 17) | ((uint32_t)(LM_BM >> 4) << 24);
+                              ((uint32_t)(LM_BN >> 3) << 17) | ((uint32_t)((2 * LM_BM) >> 4) << 24);
 
 __device__ __forceinline__ void lm_mma(uint32_t tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  ::"r"(tmem), "l"(adesc), "l"(bdesc), "r"(LM_IDESC), "r"(accumulate)
                  : "memory");
 }
-// arrive on bar once every tcgen05.mma issued so far by this thread completes
-__device__ __forceinline__ void lm_commit(uint64_t* bar)
+// arrive on the mbarrier at cluster address bar once every MMA issued so far
+// by this thread completes
+__device__ __forceinline__ void lm_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(smem_u32(bar)) : "memory");
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
 }
-// the same, arriving on the mbarrier at bar's offset in every CTA of cta_mask
-__device__ __forceinline__ void lm_commit_mc(uint64_t* bar, uint16_t cta_mask)
+// arrive on the mbarrier at cluster address bar (either CTA of the pair)
+__device__ __forceinline__ void lm_arrive_cluster(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%0], %1;" ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void cluster_sync()
 {
@@ -139,45 +146,48 @@ __device__ __forceinline__ void lm_ld32(uint32_t taddr, uint32_t (&v)[32])
 }
 
 // ------------------------------------------------------------------------- //
-// k_lmhead: persistent two-CTA clusters; cluster c takes the tiles c, c + C, //
-// c + 2C, ... of (pairs of 128-row blocks) x (256-column blocks)            //
+// k_lmhead: persistent CTA pairs; pair c takes the tiles c, c + C, c + 2C,   //
+// ... of (256-row blocks of H) x (256-column blocks of W)                    //
 // ------------------------------------------------------------------------- //
 __global__ void __launch_bounds__(LM_THREADS, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
              float* __restrict__ out, int M, int N, int K, int64_t ldo, unsigned* err, LmStats st)
 {
     extern __shared__ unsigned char lm_smem_raw[];
-    __shared__ __align__(8) uint64_t full[LM_STAGES];   // stage loaded (own H + both W halves)
-    __shared__ __align__(8) uint64_t empty[LM_STAGES];  // stage read by both CTAs' MMAs
-    __shared__ __align__(8) uint64_t acc_full[2];       // accumulator complete
-    __shared__ __align__(8) uint64_t acc_empty[2];      // accumulator read back
+    __shared__ __align__(8) uint64_t full[LM_STAGES];   // even CTA: the stage holds both CTAs' boxes
+    __shared__ __align__(8) uint64_t empty[LM_STAGES];  // the MMAs have read this CTA's stage
+    __shared__ __align__(8) uint64_t acc_full[2];       // the accumulator is complete
+    __shared__ __align__(8) uint64_t acc_empty[2];      // even CTA: both CTAs read the accumulator back
     __shared__ uint32_t tmem_slot;
     __shared__ int failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
     // stage buffers on a 1024-byte boundary (the period of the 128-byte
-    // swizzle); the offset is the same in both CTAs of the cluster
+    // swizzle); the offset is the same in both CTAs of the pair, which the
+    // 2-SM MMA needs (one descriptor addresses both CTAs' operands)
     const uint32_t raw = smem_u32(lm_smem_raw);
     unsigned char* base = lm_smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const int nk = (K + LM_BK - 1) / LM_BK;
-    const int n_mpair = ((M + LM_BM - 1) / LM_BM + 1) / 2;
+    const int n_mpair = (M + 2 * LM_BM - 1) / (2 * LM_BM);
     const int n_tiles = n_mpair * ((N + LM_BN - 1) / LM_BN);
     const int cid = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
     const volatile int* vfailed = &failed;
 
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+        // both CTAs of the pair allocate together (the same columns in each)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(&tmem_slot)), "r"(LM_TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     if (threadIdx.x == 32) {
         for (int s = 0; s < LM_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);  // one commit from each CTA's MMA issuer
+            mbar_init(&full[s], 1);   // the even CTA's producer (with both CTAs' bytes)
+            mbar_init(&empty[s], 1);  // one commit of the MMA issuer
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 4);  // lane 0 of each epilogue warp
+            mbar_init(&acc_empty[a], 8);  // lane 0 of each epilogue warp of both CTAs
         }
         failed = 0;
         fence_barrier_init();
@@ -189,11 +199,12 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     const uint32_t tmem = tmem_slot;
 
     if (threadIdx.x == 0) {
-        // ---------------- producer: K slices of H and W into the ring
+        // ---------------- producer (both CTAs): this CTA's half of each K slice
+        const uint64_t pol_w = l2_evict_first(), pol_h = l2_evict_last();
         uint32_t it = 0;
         for (int t = cid; t < n_tiles && !*vfailed; t += n_cl) {
             const int m0 = ((t % n_mpair) * 2 + (int)rank) * LM_BM;
-            const int n0 = (t / n_mpair) * LM_BN;
+            const int n0 = (t / n_mpair) * LM_BN + (int)rank * LM_BNH;
             for (int kt = 0; kt < nk; ++kt, ++it) {
                 const uint32_t s = it % LM_STAGES;
                 if (it >= LM_STAGES && !lm_wait(&empty[s], ((it / LM_STAGES) - 1) & 1, vfailed)) {
@@ -202,21 +213,22 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                 }
                 unsigned char* a = base + s * LM_STAGE_BYTES;
                 unsigned char* b = a + LM_A_BYTES;
-                mbar_arrive_expect_tx(&full[s], LM_STAGE_BYTES);
-                tma_load_2d(a, &tmap_h, kt * LM_BK, m0, &full[s]);
-#pragma unroll
-                for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)
-                    tma_load_2d_mc(b + j * LM_BOX_B, &tmap_w, n0 + 64 * j, kt * LM_BK, &full[s], 0x3);
+                const uint32_t fb = lm_mapa(&full[s], 0);
+                if (leader) mbar_arrive_expect_tx(&full[s], 2 * LM_STAGE_BYTES);
+                lm_tma_2d(a, &tmap_h, kt * LM_BK, m0, fb, pol_h);
+                lm_tma_2d(b, &tmap_w, n0, kt * LM_BK, fb, pol_w);
+                lm_tma_2d(b + LM_BOX_B, &tmap_w, n0 + 64, kt * LM_BK, fb, pol_w);
             }
         }
-        // drain: every stage this CTA filled has been read by both MMAs, so
-        // no commit of the peer is still on its way to this CTA's barriers
+        // drain: every stage this CTA filled has been read by the MMAs, so
+        // no copy or commit is still on its way to either CTA's barriers
         for (uint32_t i = it; i < it + LM_STAGES && !*vfailed; ++i)
             if (i >= LM_STAGES && !lm_wait(&empty[i % LM_STAGES], ((i / LM_STAGES) - 1) & 1, vfailed))
                 failed = 1;
-    } else if (threadIdx.x == 32) {
-        // ---------------- MMA issuer
+    } else if (threadIdx.x == 32 && leader) {
+        // ---------------- MMA issuer (even CTA)
         uint32_t it = 0, ti = 0;
+        const uint32_t peer = 1;
         for (int t = cid; t < n_tiles && !*vfailed; t += n_cl, ++ti) {
             const uint32_t acc = ti & 1;
             if (ti >= 2 && !lm_wait(&acc_empty[acc], ((ti >> 1) - 1) & 1, vfailed)) {
@@ -243,9 +255,13 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                     const uint64_t bd = lm_sdesc(b + kk * 2048, LM_BOX_B, 1024);
                     lm_mma(d, ad, bd, (kt | kk) != 0 ? 1u : 0u);
                 }
-                lm_commit_mc(&empty[s], 0x3);  // the stage is free in both CTAs once read
+                // the stage is free in both CTAs once the MMAs have read it
+                lm_commit(smem_u32(&empty[s]));
+                lm_commit(lm_mapa(&empty[s], peer));
             }
-            lm_commit(&acc_full[acc]);  // the accumulator is complete (or the loop gave up)
+            // the accumulator is complete (or the loop gave up) in both CTAs
+            lm_commit(smem_u32(&acc_full[acc]));
+            lm_commit(lm_mapa(&acc_full[acc], peer));
         }
     } else if (warp >= 2) {
         // ---------------- epilogue: warp w reads accumulator lanes 32 (w % 4) ..
@@ -311,15 +327,16 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) lm_arrive_cluster(lm_mapa(&acc_empty[acc], 0));
         }
     }
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0 && failed && err) atomicOr(err, 8u);  // a bounded wait ran out
-    cluster_sync();  // neither CTA leaves while the other may still reach its memory
+    cluster_sync();  // neither CTA leaves (or frees its tensor memory) while the other may still reach it
+    tc_fence_after();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LM_TMEM_COLS)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LM_TMEM_COLS)
                      : "memory");
 }
 
@@ -372,7 +389,7 @@ bool lmhead_shape_ok(const void* hidden, const void* w, int M, int N, int K)
 cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, int N, int K, int64_t ldo,
                           unsigned* err, cudaStream_t s, const LmStats& st)
 {
-    static int max_clusters = 0;
+    static DeviceOnce once;  // per device: the shared-memory opt-in and the resident pairs
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -384,24 +401,25 @@ cudaError_t launch_lmhead(const void* hidden, const void* w, float* out, int M, 
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (max_clusters == 0) {
-        cudaError_t e = cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, LM_SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0, sms = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        cfg.gridDim = dim3((unsigned)(sms & ~1));
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_lmhead, &cfg) != cudaSuccess || n < 1) {
+    int max_clusters = 0;
+    cudaError_t e = cuda_once(once, &max_clusters, [&](int dev, int* n) {
+        cudaError_t e2 = cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, LM_SMEM);
+        if (e2 != cudaSuccess) return e2;
+        int sms = 0;
+        if ((e2 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e2;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3((unsigned)(sms & ~1));
+        if (cudaOccupancyMaxActiveClusters(n, k_lmhead, &q) != cudaSuccess || *n < 1) {
             (void)cudaGetLastError();
-            n = sms / 2;
+            *n = sms / 2;
         }
-        max_clusters = n;
-    }
+        return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
     CUtensorMap mh, mw;
     if (!bf16_map(&mh, hidden, M, K, LM_BK, LM_BM) || !bf16_map(&mw, w, K, N, 64, LM_BK))
         return cudaErrorInvalidValue;
-    const int n_mpair = ((M + LM_BM - 1) / LM_BM + 1) / 2;
+    const int n_mpair = (M + 2 * LM_BM - 1) / (2 * LM_BM);
     const int n_tiles = n_mpair * ((N + LM_BN - 1) / LM_BN);
     cfg.gridDim = dim3((unsigned)(2 * std::min(n_tiles, max_clusters)));
     return cudaLaunchKernelEx(&cfg, k_lmhead, mh, mw, out, M, N, K, ldo, err, st);

@@ -64,6 +64,8 @@ spec_status spec_verify_run_noalloc(const spec_verify_config* cfg, const spec_ve
 {
     if (!cfg || !in || !s || !out) return SPEC_ERR_INVALID_ARG;
     if (cfg->device < 0 || cfg->device >= MAX_DEVICES) return SPEC_ERR_INVALID_ARG;
+    // the fused LM head needs its fp32 logits in a workspace far larger than the array
+    if (cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD) return SPEC_ERR_UNSUPPORTED;
     if (!fits(cfg, in->batch, in->k_max)) return SPEC_ERR_INVALID_ARG;
     int prev = -1;
     if (cudaGetDevice(&prev) != cudaSuccess) return SPEC_ERR_CUDA;

@@ -165,15 +165,18 @@ template <> struct ChunkMax<float> {
 // ------------------------------------------------------------------------- //
 template <typename T, int MODE, int NTH, typename F, typename SYNC>
 __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int seg, int r, int lt,
-                                                SYNC sync, float* redf, double* redd)
+                                                SYNC sync, float* redf, double* redd,
+                                                uint32_t* hist = nullptr)
 {
     using G = SegGeom<T, NTH>;
     using CM = ChunkMax<T>;
     const int V = p.V;
     const int64_t base = (int64_t)seg * G::SEG;
-    if (MODE == SEG_CHUNK) {
+    if constexpr (MODE == SEG_CHUNK) {
         // 8 consecutive lanes hold one 128-byte chunk: its NaN-propagating max
-        // becomes a 16-bit order key (a lower bound of every key in the chunk)
+        // becomes a 16-bit order key (a lower bound of every key in the chunk).
+        // Key 0 is kept free (keys up to 0x7F all mean "no finite logit"): the
+        // fused top-k kernel takes a 0 for a chunk not streamed yet
         typename CM::P m[G::ROUNDS];
 #pragma unroll
         for (int i = 0; i < G::ROUNDS; ++i) m[i] = CM::lane(fetch(i));
@@ -188,8 +191,84 @@ __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int se
                 const int64_t e0 = base + ((int64_t)i * NTH + lt) * G::VW;
                 if (e0 < V)
                     p.chunk[(int64_t)r * p.chunk_stride + e0 / G::CHUNK_EL] =
-                        (uint16_t)(key_of(CM::value(m[i])) >> 16);
+                        (uint16_t)max(key_of(CM::value(m[i])) >> 16, 1u);
             }
+        }
+    } else if constexpr (MODE == SEG_HIST) {
+        // bf16 rows with top-p alone: the segment max M; the count of tokens
+        // at each key M16 - d, d < HIST_BINS (u8 per bin, 255 = "255 or
+        // more"), into the row's histogram area (the chunk-key area); and the
+        // sum of exp2((l - M) c) over the tokens below those keys.  The merge
+        // rebuilds the row's mass per key from the counts (equal bf16 values
+        // carry equal mass), so the nucleus cut needs no pass over the row.
+        static_assert(sizeof(T) == 2, "the key histogram is for bf16 rows");
+        const unsigned FULL = 0xffffffffu;
+        uint4 w[G::ROUNDS];
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < G::ROUNDS; ++i) {
+            w[i] = fetch(i);
+            m = fmax_nan(m, Vec16<T>::vmax(w[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(FULL, m, o));
+        sync();  // the previous segment's reductions and histogram are read and cleared
+        if ((lt & 31) == 0) redf[lt >> 5] = m;
+        sync();
+        float M = redf[0];
+#pragma unroll
+        for (int i = 1; i < NTH / 32; ++i) M = fmax_nan(M, redf[i]);
+        float s = 0.f;
+        if (M > -INFINITY && M < INFINITY) {
+            const uint32_t m16 = key16_bf16(__float_as_uint(M) >> 16);
+            // the lowest value counted (keys below 0x80 are -inf and NaNs)
+            const uint32_t lo16 = m16 >= 0x7Fu + (HIST_BINS - 1) ? m16 - (HIST_BINS - 1) : 0x7Fu;
+            const uint32_t thr = __float_as_uint(val_key16(lo16)) >> 16;
+            const uint32_t thr2 = thr | (thr << 16);
+            const float c = p.c, Mc = M * p.c;
+#pragma unroll
+            for (int i = 0; i < G::ROUNDS; ++i) {
+                const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t x = ws[h];
+                    const uint32_t in = ChunkMax<__nv_bfloat16>::ge2(x, thr2);  // 0xFFFF per counted half
+                    const float elo = ex2_fast(fmaf(bf16_lo(x), c, -Mc));
+                    const float ehi = ex2_fast(fmaf(bf16_hi(x), c, -Mc));
+                    s += (in & 0xFFFFu) ? 0.f : elo;
+                    s += (in >> 16) ? 0.f : ehi;
+                    if (in) {
+                        if (in & 0xFFFFu) atomicAdd(&hist[m16 - key16_bf16(x & 0xFFFFu)], 1u);
+                        if (in >> 16) atomicAdd(&hist[m16 - key16_bf16(x >> 16)], 1u);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+        if ((lt & 31) == 0) redd[lt >> 5] = (double)s;
+        sync();
+        // the counts out, four u8 bins per word (saturating), and cleared
+        uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.chunk) +
+                                                    (int64_t)r * p.chunk_stride * 2 + (int64_t)seg * HIST_BINS);
+        for (int q = lt; q < HIST_BINS / 4; q += NTH) {
+            uint32_t word = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                word |= min(hist[4 * q + j], 255u) << (8 * j);
+                hist[4 * q + j] = 0u;
+            }
+            out[q] = word;
+        }
+        if (lt == 0) {
+            double tot = 0.0;
+#pragma unroll
+            for (int i = 0; i < NTH / 32; ++i) tot += redd[i];
+            SegStat st;
+            st.m = M;
+            st.pad = 0.f;
+            st.s = tot;
+            p.seg[(int64_t)r * p.nseg + seg] = st;
         }
     } else {
         // one read of the thread's words; each warp's (max, sum exp) in fp32
@@ -702,6 +781,173 @@ __device__ bool fast_topk(const Params& p, const T* row, int r, unsigned char* s
 }
 
 // ------------------------------------------------------------------------- //
+// the nucleus of a bf16 row from its per-segment key histograms (SEG_HIST)  //
+// ------------------------------------------------------------------------- //
+// sum over the row of exp2((l - M) c), read from L2 / HBM (NT threads)
+template <typename T>
+__device__ double row_sumexp(const T* row, int V, float M, float c, double* red)
+{
+    float s = 0.f;
+    for (int e = threadIdx.x; e < V; e += NT) s += ex2_fast((Elem<T>::load_cg(row, e) - M) * c);
+    return block_sum_d((double)s, red);
+}
+
+// exp2((v - M) c) for the bf16 value of key k: the exponent in two parts (c +
+// c_lo) so that it is exact to ~2^-40, its fractional part through exp2f
+__device__ __forceinline__ float hist_weight(const Params& p, uint32_t k, float M)
+{
+    const float d = val_key16(k) - M;  // exact: two bf16 values
+    if (!(d > -INFINITY)) return 0.f;
+    const float x = d * p.c;
+    const float x_lo = fmaf(d, p.c, -x) + d * p.c_lo;  // the rounding of d c, and d c_lo
+    const float n = rintf(x);
+    return ldexpf(exp2f((x - n) + x_lo), (int)n);
+}
+
+// Finds the nucleus (top-p after temperature, no top-k) of row r from the
+// segments' key histograms: the row's count per key in the HIST_BINS keys
+// below its max, each key's mass count x exp2((v - M) c), the tokens below
+// that window from the segments' partial sums; the rank prefix is cut where
+// the mass before a token reaches top_p.  Ties at the cut key are kept in
+// ascending id, found in the one segment that holds the boundary token.
+// Returns 0 with st complete (MODE_PREFIX; the caller builds a list if small),
+// 1 when the cut lies below the window (st.S then holds the row's total), 2
+// when a bin saturated (the caller recomputes everything).  NT threads.
+template <typename T>
+__device__ int merge_row_hist(const Params& p, const T* row, int r, RowStat& st, unsigned char* scratch)
+{
+    static_assert(HIST_BINS == NT, "one row bin per thread");
+    __shared__ double s_redd[NT / 32 + 1];
+    __shared__ int s_redi[NT / 32 + 1];
+    __shared__ int s_flag;
+    __shared__ int s_cut;
+    __shared__ double s_above;
+    __shared__ int s_cnt_above;
+    __shared__ int s_seg;
+    __shared__ int s_before;
+    __shared__ int s_id;
+    __shared__ int s_cntk;
+    const int t = threadIdx.x;
+    const float M = st.M;
+    const uint32_t M16 = key16_bf16(__float_as_uint(M) >> 16);
+    const uint8_t* H = reinterpret_cast<const uint8_t*>(p.chunk) + (int64_t)r * p.chunk_stride * 2;
+    const SegStat* segs = p.seg + (int64_t)r * p.nseg;
+    uint32_t cnt = 0;      // tokens at key M16 - t
+    double below = 0.0;    // mass of this thread's share of the tokens below the window
+    bool sat = false;
+    for (int s = 0; s < p.nseg; ++s) {
+        const float ms = __ldcg(&segs[s].m);
+        if (!(ms > -INFINITY)) continue;  // every token -inf
+        const uint32_t m16 = key16_bf16(__float_as_uint(ms) >> 16);
+        const uint32_t off = M16 - m16;  // the segment's window starts off keys below the row's
+        if ((uint32_t)t >= off) {
+            const uint32_t c = __ldcg(H + (int64_t)s * HIST_BINS + (t - off));
+            sat |= c == 255u;
+            cnt += c;
+        }
+        if (off + (uint32_t)t >= (uint32_t)HIST_BINS) {
+            const uint32_t c = __ldcg(H + (int64_t)s * HIST_BINS + t);
+            sat |= c == 255u;
+            if (c) below += (double)c * (double)hist_weight(p, m16 - (uint32_t)t, M);
+        }
+        if (t == 0) below += __ldcg(&segs[s].s) * (double)exp2f((ms - M) * p.c);
+    }
+    if (csync_or(sat, &s_flag)) return 2;
+    const uint32_t key = M16 - (uint32_t)t;
+    const float w = key >= 0x80u ? hist_weight(p, key, M) : 0.f;
+    const double mass = (double)cnt * (double)w;
+    double tot;
+    const double cum_ex = block_excl_scan<double>(mass, s_redd, &tot);
+    const double S_all = tot + block_sum_d(below, s_redd);
+    const double target = (double)p.top_p * S_all;
+    if (t == 0) s_cut = -1;
+    csync();
+    // the first key whose inclusive mass reaches the target (strict rule:
+    // a token is kept while the mass before it is below top_p)
+    if (cum_ex < target && cum_ex + mass >= target && cnt > 0) {
+        s_cut = t;
+        s_above = cum_ex;
+    }
+    int n_above_total;
+    const int n_before = block_excl_scan<int>((int)cnt, s_redi, &n_above_total);
+    csync();
+    const int cut = s_cut;
+    if (cut < 0) {
+        st.S = S_all;
+        return 1;
+    }
+    if (t == cut) s_cnt_above = n_before;
+    csync();
+    (void)n_above_total;
+    const uint32_t kap16 = M16 - (uint32_t)cut;
+    const float wk = hist_weight(p, kap16, M);
+    const double above = s_above;
+    if (t == cut) s_cntk = (int)cnt;
+    csync();
+    const int cntk = s_cntk;
+    const double q = (target - above) / (double)wk;
+    int nk = (int)ceil(q);
+    nk = max(1, min(nk, cntk));
+    int32_t ik = p.V - 1;
+    if (nk < cntk) {
+        // the nk-th token of key kap16 in ascending id: which segment holds it
+        // (its count of that key is a bin of its histogram), then a walk of
+        // that segment in id order
+        using G = SegGeom<T, NT>;
+        int cs = 0;
+        if (t < p.nseg) {
+            const float ms = __ldcg(&segs[t].m);
+            if (ms > -INFINITY) {
+                const uint32_t m16 = key16_bf16(__float_as_uint(ms) >> 16);
+                if (m16 >= kap16 && m16 - kap16 < (uint32_t)HIST_BINS)
+                    cs = (int)__ldcg(H + (int64_t)t * HIST_BINS + (m16 - kap16));
+            }
+        }
+        static_assert(NT >= 64, "segments of a row fit one thread each up to NT");
+        int dummy;
+        const int cb = block_excl_scan<int>(cs, s_redi, &dummy);
+        if (t < p.nseg && cb < nk && nk <= cb + cs) {
+            s_seg = t;
+            s_before = cb;
+        }
+        csync();
+        const int sseg = s_seg;
+        const int need = nk - s_before;  // 1-based rank of the boundary token in the segment
+        const int e_begin = sseg * G::SEG;
+        const int e_end = min(p.V, e_begin + G::SEG);
+        constexpr int EPT = G::SEG / NT;  // contiguous elements per thread
+        const int e0 = e_begin + t * EPT;
+        int mine = 0;
+        for (int i = 0; i < EPT; ++i) {
+            const int e = e0 + i;
+            if (e < e_end && key16_bf16((uint32_t)__ldcg((const unsigned short*)row + e)) == kap16) ++mine;
+        }
+        const int mb = block_excl_scan<int>(mine, s_redi, &dummy);
+        if (t == 0) s_id = p.V - 1;
+        csync();
+        if (mb < need && need <= mb + mine) {
+            int seen = mb;
+            for (int i = 0; i < EPT; ++i) {
+                const int e = e0 + i;
+                if (e < e_end && key16_bf16((uint32_t)__ldcg((const unsigned short*)row + e)) == kap16 &&
+                    ++seen == need) {
+                    s_id = e;
+                    break;
+                }
+            }
+        }
+        csync();
+        ik = s_id;
+    }
+    st.mode = MODE_PREFIX;
+    st.kappa = key_of(val_key16(kap16));
+    st.i_kappa = ik;
+    st.n_kept = s_cnt_above + nk;
+    st.S = above + (double)nk * (double)wk;
+    return 0;
+}
+
+// ------------------------------------------------------------------------- //
 // row merge: statistics and kept set of row slot r                          //
 // ------------------------------------------------------------------------- //
 template <typename T>
@@ -752,6 +998,24 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
             st.S = block_sum_d(s, s_redd);
             have_stats = true;
             if (!topk_on && !topp_on) done = true;  // MODE_ALL
+            if constexpr (sizeof(T) == 2) if (p.seg_mode == SEG_HIST && topp_on && !topk_on) {
+                // the segment records hold only the mass below each key window:
+                // the histograms give the rest and the nucleus itself
+                const int h = merge_row_hist<T>(p, row, r, st, scratch);
+                if (h == 0) {
+                    if (st.n_kept <= KCAP) {  // a small nucleus becomes a list (one pass)
+                        double S;
+                        const int nk = collect_prefix<T>(row, V, st, st.M, c, kid, kl, &S);
+                        st.S = S;
+                        st.n_kept = nk;
+                        st.mode = MODE_LIST;
+                    }
+                    done = true;
+                } else if (h == 2) {
+                    st.S = row_sumexp<T>(row, V, st.M, c, s_redd);  // a bin saturated: the plain sum
+                }
+                // h == 1: st.S is the row's total; the radix descent below finds the cut
+            }
         }
     }
 
@@ -1279,8 +1543,11 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     __shared__ Ring ring;
     __shared__ float s_redf[NS / 32 + 1];
     __shared__ double s_redd[NS / 32 + 1];
+    __shared__ uint32_t s_hist[MODE == SEG_HIST ? HIST_BINS : 1];
     using G = SegGeom<T, NS>;
     const int tid = threadIdx.x;
+    if (MODE == SEG_HIST)
+        for (int i = tid; i < HIST_BINS; i += STREAM_THREADS) s_hist[i] = 0u;
     // the merge kernel that follows may be scheduled as this grid drains; it
     // waits for this grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1298,6 +1565,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     if (tid >= NS) {
         // ---------------- producer
         if (tid != NS) return;
+        if (p.stall) return;  // fault injection: no copy, so every consumer wait runs out
         const uint64_t pol = l2_evict_first();  // the rows are read once; the chunk keys stay in L2
         int k = 0;
         bool failed = false;
@@ -1342,8 +1610,8 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     // ---------------- stream threads
     for (int k = 0;; ++k) {
         const int s = k % NSTAGE;
-        if (!mbar_wait(&ring.full[s], (k / NSTAGE) & 1)) {
-            atomicOr(p.err, 2u);
+        if (!ssync_and(mbar_wait_n(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
+            if (tid == 0) atomicOr(p.err, 2u);
             break;
         }
         const int item = ring.item[s];
@@ -1357,7 +1625,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
                 const int64_t e0 = base + ((int64_t)i * NS + tid) * G::VW;
                 return e0 < p.V ? sv4[i * NS + tid] : Vec16<T>::neg_inf();
             },
-            seg, r, tid, [] { ssync(); }, s_redf, s_redd);
+            seg, r, tid, [] { ssync(); }, s_redf, s_redd, s_hist);
         ssync();  // every stream thread is done with the stage
         if (tid == 0) mbar_arrive(&ring.empty[s]);
     }
@@ -1389,6 +1657,7 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 #include "sv_warp.cuh"
 #include "sv_mcand.cuh"
 #include "sv_exit.cuh"
+#include "sv_fused.cuh"
 
 namespace sv {
 
@@ -1407,13 +1676,11 @@ static cudaError_t launch_rows_t(const Params& p, cudaStream_t s)
 template <typename T, int MODE>
 static cudaError_t launch_stream_t(const Params& p, int ctas, cudaStream_t s)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_stream<T, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static DeviceOnce once;  // the shared-memory opt-in, per device
+    const cudaError_t e = cuda_once(once, nullptr, [](int, int*) {
+        return cudaFuncSetAttribute(k_stream<T, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, STREAM_SMEM);
+    });
+    if (e != cudaSuccess) return e;
     k_stream<T, MODE><<<ctas, STREAM_THREADS, STREAM_SMEM, s>>>(p);
     return cudaGetLastError();
 }
@@ -1450,13 +1717,11 @@ template <typename T>
 static cudaError_t launch_merge_warp_t(const Params& p, cudaStream_t s)
 {
     const int64_t rows = (int64_t)p.B * p.rps;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e0 = cudaFuncSetAttribute(k_merge_warp<T>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, WM_SMEM);
-        if (e0 != cudaSuccess) return e0;
-        attr = true;
-    }
+    static DeviceOnce once;  // the shared-memory opt-in, per device
+    const cudaError_t e0 = cuda_once(once, nullptr, [](int, int*) {
+        return cudaFuncSetAttribute(k_merge_warp<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, WM_SMEM);
+    });
+    if (e0 != cudaSuccess) return e0;
     cudaError_t e = launch_dependent(k_merge_warp<T>, p, (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
                                      WM_WARPS * 32, WM_SMEM, s);
     if (e != cudaSuccess) return e;
@@ -1469,6 +1734,18 @@ static cudaError_t launch_merge_topk_t(const Params& p, cudaStream_t s)
     cudaError_t e = launch_dependent(k_merge_cand<T>, p, (unsigned)(p.B * p.rps), MC_T, 0, s);
     if (e != cudaSuccess) return e;
     return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
+}
+
+cudaError_t launch_verify_topk(const Params& p, int dtype, int num_sms, cudaStream_t s)
+{
+    return dtype == 1 ? launch_verify_topk_t<__nv_bfloat16>(p, num_sms, s)
+                      : launch_verify_topk_t<float>(p, num_sms, s);
+}
+
+cudaError_t launch_decide(const Params& p, int dtype, cudaStream_t s)
+{
+    return dtype == 1 ? launch_dependent(k_decide<__nv_bfloat16>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s)
+                      : launch_dependent(k_decide<float>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
 }
 
 cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s)
@@ -1494,6 +1771,8 @@ cudaError_t launch_rows(const Params& p, int dtype, bool vec, cudaStream_t s)
 cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_t s)
 {
     if ((int64_t)p.B * p.rps * p.nseg <= 0) return cudaSuccess;
+    if (p.seg_mode == SEG_HIST)
+        return dtype == 1 ? launch_stream_t<__nv_bfloat16, SEG_HIST>(p, ctas, s) : cudaErrorInvalidValue;
     const bool chunk = p.seg_mode == SEG_CHUNK;
     if (dtype == 1)
         return chunk ? launch_stream_t<__nv_bfloat16, SEG_CHUNK>(p, ctas, s)

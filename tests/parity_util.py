@@ -32,8 +32,9 @@ def oracle_tokens(orc, w, *, draft_kind=None, delta=DELTA):
     """Drafted tokens from the oracle's draft-side sampler (tag-1 uniforms)."""
     dk = orc.DRAFT_PROBS if (draft_kind or w.draft_kind) == "probs" else orc.DRAFT_LOGITS
     toks, margin = orc.draft_sample(w.draft, w.k_per_row, draft_kind=dk,
-                                    temperature=w.temperature, top_k=w.top_k, top_p=w.top_p,
-                                    seed=w.seed, round=w.round, delta=delta)
+                                    temperature=abi_float(w.temperature), top_k=w.top_k,
+                                    top_p=abi_float(w.top_p), seed=w.seed, round=w.round,
+                                    delta=delta)
     return toks, margin
 
 
@@ -62,21 +63,51 @@ def run_gpu(w, toks, *, verifier=None, seed=None, round=None, repeat=1, early_ex
     return outs[0] if repeat == 1 else outs
 
 
+def abi_float(x: float) -> float:
+    """A knob as the C ABI carries it: spec_sampling holds temperature and
+    top_p as fp32, so the oracle is given the same (fp32-rounded) numbers."""
+    return float(np.float32(x))
+
+
 def run_oracle(orc, w, toks, b_begin=0, b_end=None, delta=DELTA):
     dk = orc.DRAFT_PROBS if w.draft_kind == "probs" else orc.DRAFT_LOGITS
     return orc.verify(w.target, w.draft, toks, w.k_per_row, draft_kind=dk,
-                      temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, seed=w.seed,
-                      round=w.round, delta=delta, b_begin=b_begin, b_end=b_end)
+                      temperature=abi_float(w.temperature), top_k=w.top_k,
+                      top_p=abi_float(w.top_p), seed=w.seed, round=w.round, delta=delta,
+                      b_begin=b_begin, b_end=b_end)
 
 
-def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL, early_exit=False):
+def run_oracle_parallel(orc, w, toks, delta=DELTA, chunk=4, workers=None):
+    """The oracle over every sequence, split into ranges of ``chunk`` sequences
+    verified by a pool of threads.  Each call is the single-threaded C oracle
+    (ctypes releases the interpreter lock while it runs, and the oracle keeps
+    no global state), so the ranges run in parallel on the host cores; the
+    outputs of each range are copied into one result."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    ranges = [(b, min(w.B, b + chunk)) for b in range(0, w.B, chunk)]
+    n = workers or max(1, min(len(ranges), os.cpu_count() or 1))
+    with ThreadPoolExecutor(n) as ex:
+        parts = list(ex.map(lambda r: (r, run_oracle(orc, w, toks, r[0], r[1], delta=delta)),
+                            ranges))
+    out = {k: v.copy() for k, v in parts[0][1].items()}
+    for (b0, b1), part in parts[1:]:
+        for k in out:
+            out[k][b0:b1] = part[k][b0:b1]
+    return out
+
+
+def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL, early_exit=False,
+            delta_topp=None):
     """Assert parity on the sequences ``rows``; returns the near-tie count.
     early_exit: the per-slot outputs exist only for the positions read (up to
     the first rejection): they are compared there and must be NaN beyond;
-    alpha is not computed."""
+    alpha is not computed.  delta_topp: the window of the top-p prefix gaps
+    when the path's nucleus arithmetic allows a narrower one than delta."""
     import oracle as O
     rows = np.arange(w.B) if rows is None else np.asarray(rows)
-    near = (o["margin_accept"] < delta) | (o["margin_topp"] < delta) | (o["margin_cdf"] < delta)
+    dtp = delta if delta_topp is None else delta_topp
+    near = (o["margin_accept"] < delta) | (o["margin_topp"] < dtp) | (o["margin_cdf"] < delta)
     n_near = 0
     for b in rows:
         st_o, st_g = int(o["row_status"][b]), int(g["row_status"][b])
@@ -114,8 +145,8 @@ def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL, early_ex
             if "p_t_at_draft" in g:
                 # a row whose nucleus boundary lies inside the window may keep one
                 # boundary token more or less: its probabilities are not compared
-                sure_t = o["topp_margin_t"][b, :kb + 1] >= delta
-                sure = sure_t[:kb] & (o["topp_margin_d"][b, :kb] >= delta)
+                sure_t = o["topp_margin_t"][b, :kb + 1] >= dtp
+                sure = sure_t[:kb] & (o["topp_margin_d"][b, :kb] >= dtp)
                 for name in ("p_t_at_draft", "p_d_at_draft"):
                     np.testing.assert_allclose(g[name][b, :kb][sure], o[name][b, :kb][sure],
                                                rtol=prob_rtol, atol=PROB_ATOL,
@@ -129,7 +160,7 @@ def compare(g, o, w, toks, rows=None, delta=DELTA, prob_rtol=PROB_RTOL, early_ex
                                            err_msg=f"residual mass sequence {b}")
             if "alpha" in g:
                 # alpha_j = sum_v min(p_t, p_d): each term in fp32, summed exactly
-                sure = (o["topp_margin_t"][b, :kb] >= delta) & (o["topp_margin_d"][b, :kb] >= delta)
+                sure = (o["topp_margin_t"][b, :kb] >= dtp) & (o["topp_margin_d"][b, :kb] >= dtp)
                 np.testing.assert_allclose(g["alpha"][b, :kb][sure], o["alpha"][b, :kb][sure],
                                            rtol=prob_rtol, atol=1e-7, err_msg=f"alpha sequence {b}")
                 assert np.all(np.isnan(g["alpha"][b, kb:]))

@@ -8,7 +8,7 @@ parity against the oracle verifying the same (GPU) logits."""
 import numpy as np
 import pytest
 
-from parity_util import DELTA, compare, run_oracle, to_device
+from parity_util import DELTA, compare, run_oracle, run_oracle_parallel, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -84,15 +84,16 @@ def test_lmhead_config5_shape(orc):
     assert float(diff.max()) < 2e-3, float(diff.max())
 
 
-def test_fused_verify_config5_reduced(orc):
-    """The fused round (LM head + verify, draft probabilities) on the config-5
-    recipe at B = 8: tokens, statuses and probabilities against the oracle
-    verifying the GPU's own logits."""
+def test_fused_verify_config5_full(orc):
+    """The fused round (LM head + verify, draft probabilities) of the config-5
+    workload at its full batch, B = 32: tokens, statuses and probabilities of
+    every sequence against the oracle verifying the GPU's own logits (the
+    oracle's fp64 LM head is pinned separately above)."""
     import torch
     import speculative_decoding_verification_42_gb300 as sv
-    from workloads.synth import make_lmhead_workload
-    B, K, V, H = 8, 7, 128256, 8192
-    w5 = make_lmhead_workload("fused B=8", B=B, K_max=K, V=V, H=H, temperature=0.8, seed=4)
+    from workloads import make_config
+    w5 = make_config(5)
+    B, K, V, H = w5.B, w5.K_max, w5.V, w5.hidden.shape[1]
     g, h, w = _gpu_logits(w5.hidden, w5.w_vocab)
     logits = g.cpu().numpy().reshape(B, K + 1, V)
     # draft probabilities: softmax((target logits + noise) / T), as the recipe says
@@ -112,6 +113,11 @@ def test_fused_verify_config5_reduced(orc):
     torch.cuda.synchronize()
     gout = {k: v.cpu().numpy() for k, v in out.items()}
     ver.close()
-    o = run_oracle(orc, w5, toks)
+    o = run_oracle_parallel(orc, w5, toks)
     n_near = compare(gout, o, w5, toks)
-    assert n_near <= 1
+    why = {k: int((o[k] < DELTA).sum()) for k in ("margin_accept", "margin_topp", "margin_cdf")}
+    print(f"fused round B={B}: {B - n_near} of {B} sequences bit-exact; near-ties {why}")
+    # without knobs the sample is an inverse CDF over all 128256 tokens, whose
+    # masses are ~1e-5 of Z each: a CDF gap falls within 1e-6 Z of the target
+    # in about a fifth of the sequences
+    assert n_near <= 0.4 * B, why

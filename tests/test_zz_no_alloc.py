@@ -13,7 +13,7 @@ import ctypes as C
 import numpy as np
 import pytest
 
-from parity_util import PROB_RTOL, oracle_tokens, to_device
+from parity_util import PROB_RTOL, compare, oracle_tokens, run_oracle, to_device
 from workloads import make_workload
 
 pytestmark = pytest.mark.gpu
@@ -85,6 +85,10 @@ def test_noalloc_equals_handle_entry_point_twice(orc, lib, knobs, dtype, V):
                                        rtol=PROB_RTOL, atol=1e-9, equal_nan=True,
                                        err_msg=f"{f}, call with round {round_}")
         assert (got["num_accepted"] >= 0).all()
+        # and against the fp64 oracle on the same bytes
+        w.round = round_
+        g = {f: got[f].cpu().numpy() for f in OUT_FIELDS}
+        assert compare(g, run_oracle(orc, w, toks_np), w, toks_np) <= 1
     ver.close()
 
 
@@ -102,3 +106,9 @@ def test_noalloc_rejects_sizes_beyond_its_array(lib):
     outs = sv.spec_verify_outputs(16, 16, None, None, None, None, None)
     rc = L.spec_verify_run_noalloc(C.byref(cfg), C.byref(ins), C.byref(s), C.byref(outs), None)
     assert rc == sv.SPEC_ERR_INVALID_ARG
+    # the fused LM head is not served without a workspace of its own
+    cfg.target_kind, cfg.target_dtype, cfg.hidden = sv.SPEC_TARGET_HIDDEN_LMHEAD, sv.SPEC_BF16, 64
+    cfg.draft_kind, cfg.draft_dtype = sv.SPEC_DRAFT_PROBS, sv.SPEC_F32
+    ins = sv.spec_verify_inputs(16, 16, 16, 16, None, 1, 1)
+    rc = L.spec_verify_run_noalloc(C.byref(cfg), C.byref(ins), C.byref(s), C.byref(outs), None)
+    assert rc == sv.SPEC_ERR_UNSUPPORTED
