@@ -905,6 +905,10 @@ __device__ int merge_row_hist(const Params& p, const T* row, int r, RowStat& st,
         }
         static_assert(NT >= 64, "segments of a row fit one thread each up to NT");
         int dummy;
+        if (t == 0) {
+            s_seg = 0;
+            s_before = 0;
+        }
         const int cb = block_excl_scan<int>(cs, s_redi, &dummy);
         if (t < p.nseg && cb < nk && nk <= cb + cs) {
             s_seg = t;
