@@ -693,7 +693,9 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 (arithmetic; inputs " + ("bf16 hidden/W" if fused else w.dtype) + ")",
+        # the arithmetic type of the path (bf16 inputs are widened exactly);
+        # the inputs' type is config.input_dtype
+        "dtype": "f32",
         "data": "synthetic",
         "config": cfg,
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,

@@ -170,7 +170,9 @@ int orc_row_dist(const double* l, int32_t V, double T, int32_t top_k, double top
             int32_t v = order[r].v;
             if (!keep[v]) continue;
             if (prefix < top_p) {
-                last_kept = top_p - prefix;
+                /* a rank with nothing before it (prefix exactly 0) is kept by
+                 * any top_p > 0: no rounding reaches that decision */
+                if (prefix > 0.0) last_kept = top_p - prefix;
                 prefix += e[v] / S;
             } else {
                 if (!dropped_any) first_dropped = prefix - top_p;

@@ -97,9 +97,13 @@ def test_topp_counting_definition(orc, V):
         if np.all(np.abs(mass_before[Pk > 0] - top_p) > 1e-12):
             assert np.array_equal(P > 0, kept_want), (l, T, k, top_p)
         _softmax_ratio_ok(P, l, T, P > 0)
-        # margin: distance of the boundary decisions to top_p
-        m = np.abs(mass_before[Pk > 0] - top_p)
-        assert info.topp_margin <= m.min() + 1e-12 or info.topp_margin == math.inf
+        # margin: distance of the boundary decisions to top_p; a token with no
+        # mass before it (rank 0) is kept by any top_p > 0 and has no margin
+        m = np.abs(mass_before[(Pk > 0) & (mass_before > 0)] - top_p)
+        if m.size:
+            assert info.topp_margin <= m.min() + 1e-12 or info.topp_margin == math.inf
+        else:
+            assert info.topp_margin == math.inf
 
 
 def test_topp_strict_prefix_rule_on_exact_masses(orc):
