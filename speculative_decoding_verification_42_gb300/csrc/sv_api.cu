@@ -37,6 +37,7 @@ struct spec_verify {
     unsigned* err;
     unsigned* seq_done;
     unsigned* exit_flag;  // early exit: a sequence was left to the regular pipeline
+    unsigned* work_ctr;   // [2] the fused kernel's work counter and exit ticket
     // spec_verify_set_profiling: events around the stage-1 stream kernel and
     // where each run stores the number of kernels it launched (all optional)
     cudaEvent_t prof_begin;
@@ -133,6 +134,7 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.chunk_stride = h->chunk_stride;
     p.err = h->err;
     p.seq_done = h->seq_done;
+    p.work_ctr = h->work_ctr;
 }
 
 // one workspace: 256-byte aligned sub-buffers for max_batch x max_k x vocab.
@@ -178,6 +180,7 @@ size_t layout_workspace(spec_verify* h, void* base)
     const size_t o_err = take(sizeof(unsigned));
     const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
     const size_t o_xf = take(sizeof(unsigned));
+    const size_t o_wc = take(2 * sizeof(unsigned));
     const bool lmhead = cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
     const size_t o_logits =
         lmhead ? take(sizeof(float) * (size_t)cfg->max_batch * (cfg->max_k + 1) * (size_t)V) : 0;
@@ -198,6 +201,7 @@ size_t layout_workspace(spec_verify* h, void* base)
         h->err = (unsigned*)(b + o_err);
         h->seq_done = (unsigned*)(b + o_sd);
         h->exit_flag = (unsigned*)(b + o_xf);
+        h->work_ctr = (unsigned*)(b + o_wc);
         h->logits = lmhead ? (float*)(b + o_logits) : nullptr;
     }
     return off;
@@ -575,6 +579,7 @@ spec_status spec_verify_check(spec_verify_t h, void* stream)
         cudaMemsetAsync(h->seq_ticket, 0, sizeof(unsigned) * (size_t)h->cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h->seq_done, 0, sizeof(unsigned) * (size_t)h->cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h->job_ticket, 0, sizeof(unsigned) * (size_t)h->jobs_cap, cs) != cudaSuccess ||
+        cudaMemsetAsync(h->work_ctr, 0, 2 * sizeof(unsigned), cs) != cudaSuccess ||
         cudaStreamSynchronize(cs) != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
@@ -681,7 +686,8 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
         cudaMemsetAsync(h.seq_ticket, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h.job_ticket, 0, sizeof(unsigned) * (size_t)h.jobs_cap, cs) != cudaSuccess ||
         cudaMemsetAsync(h.err, 0, sizeof(unsigned), cs) != cudaSuccess ||
-        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess)
+        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
+        cudaMemsetAsync(h.work_ctr, 0, 2 * sizeof(unsigned), cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return spec_verify_run(&h, in, s, out, stream);
 }

@@ -5,7 +5,7 @@
 // Every CTA carries three roles that run at the same time:
 //  * a producer thread (warp 8) streams the CTA's work items (row slot,
 //    segment) into a six-stage shared-memory ring with bulk copies, item =
-//    blockIdx.x + i gridDim.x, so that the rows complete in row order over
+//    from a grid-wide counter, so that the rows complete in row order over
 //    the whole stream;
 //  * four stream warps (4..7) reduce each segment to its 16-bit chunk keys
 //    (the largest logit of each 128-byte chunk);
@@ -24,15 +24,18 @@
 
 namespace sv {
 
-constexpr int FZ_NSTAGE = 6;                       // ring stages per CTA
+constexpr int FZ_NSTAGE = 4;                       // ring stages per CTA
+constexpr int FZ_GROUPS = 1;                       // stream groups: group g takes stages k = g mod FZ_GROUPS
+constexpr int FZ_GT = 128 / FZ_GROUPS;             // threads of a stream group
 constexpr int FZ_MERGE = MC_T;                     // merge threads: warps 0..3
 constexpr int FZ_STREAM0 = FZ_MERGE;               // first stream thread
 constexpr int FZ_PROD = FZ_STREAM0 + NS;           // the producer thread (warp 8, lane 0)
 constexpr int FZ_THREADS = FZ_PROD + 32;
-constexpr int FZ_CTAS_PER_SM = 2;
+constexpr int FZ_CTAS_PER_SM = 3;
 constexpr int FZ_SMEM = FZ_NSTAGE * SEG_BYTES;     // dynamic: the ring
 constexpr uint32_t FZ_POLL_LIMIT = 1u << 22;       // polls of a row's keys (about a second)
 static_assert(MC_T == 128 && NS == 128, "warps 0..3 merge, 4..7 stream");
+static_assert(FZ_NSTAGE % FZ_GROUPS == 0 && FZ_GT % 32 == 0, "a stage always belongs to one group");
 
 struct FzRing {
     uint64_t full[FZ_NSTAGE];
@@ -40,15 +43,15 @@ struct FzRing {
     int item[FZ_NSTAGE];
 };
 
-// barrier of the stream warps of the fused kernel (named barrier 3; the
+// barrier of stream group g of the fused kernel (named barrier 3 + g; the
 // merge warps use barrier 2 through the row merge's ssync)
-__device__ __forceinline__ void fz_sync() { asm volatile("bar.sync 3, %0;" ::"n"(NS) : "memory"); }
-__device__ __forceinline__ bool fz_sync_and(bool v)
+__device__ __forceinline__ void fz_sync(int g) { asm volatile("bar.sync %0, %1;" ::"r"(3 + g), "n"(FZ_GT) : "memory"); }
+__device__ __forceinline__ bool fz_sync_and(int g, bool v)
 {
     uint32_t r;
     asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-                 "bar.red.and.pred p, 3, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(r) : "r"((uint32_t)v), "n"(NS) : "memory");
+                 "bar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)v), "r"(3 + g), "n"(FZ_GT) : "memory");
     return r != 0;
 }
 
@@ -91,7 +94,12 @@ __global__ void __launch_bounds__(FZ_THREADS, FZ_CTAS_PER_SM) k_verify_topk(cons
     __shared__ FzRing ring;
     __shared__ McSmem sm;
     __shared__ int s_pending;
-    using G = SegGeom<T, NS>;
+    // the item this CTA's stream warps finished last (every CTA goes through
+    // the items at about the same pace, so it tells when a row can be near
+    // complete), and whether they are done
+    __shared__ volatile int s_stream_item;
+    __shared__ volatile int s_stream_done;   // groups done
+    using G = SegGeom<T, FZ_GT>;
     if (exit_skip(p)) return;
     // the decision grid that follows may be scheduled now; it waits for this
     // grid's completion before reading anything
@@ -102,6 +110,8 @@ __global__ void __launch_bounds__(FZ_THREADS, FZ_CTAS_PER_SM) k_verify_topk(cons
             mbar_init(&ring.empty[s], 1);
         }
         fence_barrier_init();
+        s_stream_item = -1;
+        s_stream_done = 0;
     }
     __syncthreads();  // the only barrier over all FZ_THREADS threads
     const int64_t total_items = (int64_t)p.B * p.rps * p.nseg;
@@ -110,11 +120,19 @@ __global__ void __launch_bounds__(FZ_THREADS, FZ_CTAS_PER_SM) k_verify_topk(cons
     if (threadIdx.x >= FZ_PROD) {
         // ---------------- producer
         if (threadIdx.x != FZ_PROD) return;
+        // items come from a grid-wide counter in order, so that rows complete
+        // in row order and a CTA slowed by its merges streams fewer of them;
+        // the last producer out sets the counter back to 0
         int k = 0;
         bool failed = false;
-        for (int64_t item = blockIdx.x;; item += gridDim.x) {
+        int64_t item = atomicAdd(p.work_ctr, 1u);
+        for (;; item = atomicAdd(p.work_ctr, 1u)) {
             if (item >= total_items) {
                 item = -1;
+                if (atomicAdd(p.work_ctr + 1, 1u) == gridDim.x - 1) {
+                    p.work_ctr[0] = 0u;
+                    p.work_ctr[1] = 0u;
+                }
             } else {
                 const int r = (int)(item / p.nseg);
                 const RowRef rr = row_ref(p, r);
@@ -129,7 +147,21 @@ __global__ void __launch_bounds__(FZ_THREADS, FZ_CTAS_PER_SM) k_verify_topk(cons
             }
             ring.item[s] = (int)item;
             if (item < 0) {
-                mbar_arrive(&ring.full[s]);  // the end-of-work sentinel
+                // the end-of-work sentinel, one for each group (the next
+                // FZ_GROUPS stages)
+                mbar_arrive(&ring.full[s]);
+                bool ok = true;
+                for (int g = 1; g < FZ_GROUPS && ok; ++g) {
+                    ++k;
+                    const int s2 = k % FZ_NSTAGE;
+                    if (k >= FZ_NSTAGE && !mbar_wait(&ring.empty[s2], ((k / FZ_NSTAGE) - 1) & 1)) {
+                        atomicOr(p.err, 1u);
+                        ok = false;
+                        break;
+                    }
+                    ring.item[s2] = -1;
+                    mbar_arrive(&ring.full[s2]);
+                }
                 break;
             }
             const int r = (int)(item / p.nseg), seg = (int)(item - (int64_t)r * p.nseg);
@@ -151,28 +183,39 @@ __global__ void __launch_bounds__(FZ_THREADS, FZ_CTAS_PER_SM) k_verify_topk(cons
     }
 
     if (threadIdx.x >= FZ_STREAM0) {
-        // ---------------- stream warps: chunk keys of every segment
-        const int lt = threadIdx.x - FZ_STREAM0;
-        for (int k = 0;; ++k) {
+        // ---------------- stream groups: chunk keys of every segment; group g
+        // takes the stages k = g, g + FZ_GROUPS, ...
+        const int g = (threadIdx.x - FZ_STREAM0) / FZ_GT;
+        const int lt = (threadIdx.x - FZ_STREAM0) - g * FZ_GT;
+        for (int k = g;; k += FZ_GROUPS) {
             const int s = k % FZ_NSTAGE;
-            if (!fz_sync_and(mbar_wait(&ring.full[s], (k / FZ_NSTAGE) & 1))) {
-                if (lt == 0) atomicOr(p.err, 2u);
+            if (!fz_sync_and(g, mbar_wait(&ring.full[s], (k / FZ_NSTAGE) & 1))) {
+                if (lt == 0) {
+                    atomicOr(p.err, 2u);
+                    atomicAdd((int*)&s_stream_done, 1);
+                }
                 break;
             }
             const int item = ring.item[s];
-            if (item < 0) break;
+            if (item < 0) {
+                if (lt == 0) atomicAdd((int*)&s_stream_done, 1);
+                break;
+            }
             const int r = item / p.nseg, seg = item - r * p.nseg;
             const uint4* sv4 = reinterpret_cast<const uint4*>(fz_ring_smem + (size_t)s * SEG_BYTES);
             const int64_t base = (int64_t)seg * G::SEG;
-            segment_compute<T, SEG_CHUNK, NS>(
+            segment_compute<T, SEG_CHUNK, FZ_GT>(
                 p,
                 [&](int i) {
-                    const int64_t e0 = base + ((int64_t)i * NS + lt) * G::VW;
-                    return e0 < p.V ? sv4[i * NS + lt] : Vec16<T>::neg_inf();
+                    const int64_t e0 = base + ((int64_t)i * FZ_GT + lt) * G::VW;
+                    return e0 < p.V ? sv4[i * FZ_GT + lt] : Vec16<T>::neg_inf();
                 },
-                seg, r, lt, [] { fz_sync(); }, nullptr, nullptr);
-            fz_sync();  // every stream thread is done with the stage
-            if (lt == 0) mbar_arrive(&ring.empty[s]);
+                seg, r, lt, [g] { fz_sync(g); }, nullptr, nullptr);
+            fz_sync(g);  // every thread of the group is done with the stage
+            if (lt == 0) {
+                mbar_arrive(&ring.empty[s]);
+                s_stream_item = item;
+            }
         }
         return;
     }
@@ -187,7 +230,13 @@ __global__ void __launch_bounds__(FZ_THREADS, FZ_CTAS_PER_SM) k_verify_topk(cons
             continue;
         }
         if (rr.is_draft && !drafts_streamed(p)) continue;  // probabilities (or greedy): not streamed
-        uint32_t polls = 0;
+        // until this CTA's own stream is within a round of the row's last
+        // item, the row cannot be complete: wait on shared memory only (the
+        // stream warps' waits are bounded, and they mark themselves done on
+        // every way out, so this loop ends)
+        const int last_item = (r + 1) * p.nseg - 1;
+        while (s_stream_done < FZ_GROUPS && s_stream_item + (int)gridDim.x < last_item) __nanosleep(500);
+        uint32_t polls = 0;  // the same in every merge thread from here on
         while (fz_row_pending(p, r, &s_pending)) {
             if (++polls == FZ_POLL_LIMIT) break;
             __nanosleep(256);

@@ -156,6 +156,7 @@ struct Params {
     // chunk key for a chunk not streamed yet; whoever reads a row's keys last
     // writes 0 back
     int32_t fused;
+    unsigned* work_ctr;       // [2]: the fused kernel's next work item, producers done (0 between launches)
 };
 
 constexpr int CAND_TOPK_MAX = 128;  // largest top-k the row merge of sv_mcand.cuh serves
@@ -649,7 +650,8 @@ __host__ __device__ __forceinline__ int seq_rows(const Params& p, int kb)
 __host__ __device__ __forceinline__ bool warp_merge_ok(const Params& p)
 {
     return !p.draft_launch && ((p.seg_mode == SEG_CHUNK && p.top_k <= 256 && p.nchunk <= 4096) ||
-                               (p.seg_mode == SEG_SUM && p.top_k == 0 && !(p.top_p < 1.0f)));
+                               (p.seg_mode == SEG_SUM && p.top_k == 0 && !(p.top_p < 1.0f)) ||
+                               (p.seg_mode == SEG_HIST && p.top_k == 0 && p.nseg <= 32));
 }
 cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s);
 // alpha_j = sum_v min(p_t, p_d) of every slot (when p.alpha is set)

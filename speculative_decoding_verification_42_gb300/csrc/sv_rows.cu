@@ -226,6 +226,10 @@ __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int se
             const uint32_t thr = __float_as_uint(val_key16(lo16)) >> 16;
             const uint32_t thr2 = thr | (thr << 16);
             const float c = p.c, Mc = M * p.c;
+            // pass 1, every token: exp2((l - M) c) summed over those below the
+            // window, and a bit per token inside it (bit 8 i + 2 h + half)
+            static_assert(G::ROUNDS * 8 <= 64, "a thread's tokens fit one 64-bit mask");
+            uint64_t inmask = 0ull;
 #pragma unroll
             for (int i = 0; i < G::ROUNDS; ++i) {
                 const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
@@ -233,15 +237,23 @@ __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int se
                 for (int h = 0; h < 4; ++h) {
                     const uint32_t x = ws[h];
                     const uint32_t in = ChunkMax<__nv_bfloat16>::ge2(x, thr2);  // 0xFFFF per counted half
+                    const uint32_t two = (in & 1u) | ((in >> 15) & 2u);
+                    inmask |= (uint64_t)two << (8 * i + 2 * h);
                     const float elo = ex2_fast(fmaf(bf16_lo(x), c, -Mc));
                     const float ehi = ex2_fast(fmaf(bf16_hi(x), c, -Mc));
-                    s += (in & 0xFFFFu) ? 0.f : elo;
-                    s += (in >> 16) ? 0.f : ehi;
-                    if (in) {
-                        if (in & 0xFFFFu) atomicAdd(&hist[m16 - key16_bf16(x & 0xFFFFu)], 1u);
-                        if (in >> 16) atomicAdd(&hist[m16 - key16_bf16(x >> 16)], 1u);
-                    }
+                    s += (two & 1u) ? 0.f : elo;
+                    s += (two & 2u) ? 0.f : ehi;
                 }
+            }
+            // pass 2, the tokens inside the window (a few in ten): one count each
+            while (inmask) {
+                const int bit = __ffsll((long long)inmask) - 1;
+                inmask &= inmask - 1ull;
+                const uint4 v = fetch(bit >> 3);
+                const int q = bit & 7;
+                const uint32_t word = (q & 4) ? ((q & 2) ? v.w : v.z) : ((q & 2) ? v.y : v.x);
+                const uint32_t b16 = (q & 1) ? (word >> 16) : (word & 0xFFFFu);
+                atomicAdd(&hist[m16 - key16_bf16(b16)], 1u);
             }
         }
 #pragma unroll
@@ -830,27 +842,42 @@ __device__ int merge_row_hist(const Params& p, const T* row, int r, RowStat& st,
     const int t = threadIdx.x;
     const float M = st.M;
     const uint32_t M16 = key16_bf16(__float_as_uint(M) >> 16);
-    const uint8_t* H = reinterpret_cast<const uint8_t*>(p.chunk) + (int64_t)r * p.chunk_stride * 2;
     const SegStat* segs = p.seg + (int64_t)r * p.nseg;
+    // the segment maxima, partial sums and key histograms, staged in shared
+    // memory with one round of loads
+    float* s_m = reinterpret_cast<float*>(scratch);                       // [nseg]
+    double* s_s = reinterpret_cast<double*>(scratch + 1024);              // [nseg]
+    uint8_t* Hs = scratch + 2048;                                         // [nseg][HIST_BINS]
+    static_assert(2048 + (NT / 2) * HIST_BINS <= SCRATCH_BYTES, "the histograms of a row fit the scratch");
+    {
+        const uint4* Hg = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.chunk) +
+                                                         (int64_t)r * p.chunk_stride * 2);
+        for (int i = t; i < p.nseg * (HIST_BINS / 16); i += NT) reinterpret_cast<uint4*>(Hs)[i] = __ldcg(Hg + i);
+        for (int i = t; i < p.nseg; i += NT) {
+            s_m[i] = __ldcg(&segs[i].m);
+            s_s[i] = __ldcg(&segs[i].s);
+        }
+    }
+    csync();
     uint32_t cnt = 0;      // tokens at key M16 - t
     double below = 0.0;    // mass of this thread's share of the tokens below the window
     bool sat = false;
     for (int s = 0; s < p.nseg; ++s) {
-        const float ms = __ldcg(&segs[s].m);
+        const float ms = s_m[s];
         if (!(ms > -INFINITY)) continue;  // every token -inf
         const uint32_t m16 = key16_bf16(__float_as_uint(ms) >> 16);
         const uint32_t off = M16 - m16;  // the segment's window starts off keys below the row's
         if ((uint32_t)t >= off) {
-            const uint32_t c = __ldcg(H + (int64_t)s * HIST_BINS + (t - off));
+            const uint32_t c = Hs[s * HIST_BINS + (t - off)];
             sat |= c == 255u;
             cnt += c;
         }
         if (off + (uint32_t)t >= (uint32_t)HIST_BINS) {
-            const uint32_t c = __ldcg(H + (int64_t)s * HIST_BINS + t);
+            const uint32_t c = Hs[s * HIST_BINS + t];
             sat |= c == 255u;
             if (c) below += (double)c * (double)hist_weight(p, m16 - (uint32_t)t, M);
         }
-        if (t == 0) below += __ldcg(&segs[s].s) * (double)exp2f((ms - M) * p.c);
+        if (t == 0) below += s_s[s] * (double)exp2f((ms - M) * p.c);
     }
     if (csync_or(sat, &s_flag)) return 2;
     const uint32_t key = M16 - (uint32_t)t;
@@ -896,11 +923,10 @@ __device__ int merge_row_hist(const Params& p, const T* row, int r, RowStat& st,
         using G = SegGeom<T, NT>;
         int cs = 0;
         if (t < p.nseg) {
-            const float ms = __ldcg(&segs[t].m);
+            const float ms = s_m[t];
             if (ms > -INFINITY) {
                 const uint32_t m16 = key16_bf16(__float_as_uint(ms) >> 16);
-                if (m16 >= kap16 && m16 - kap16 < (uint32_t)HIST_BINS)
-                    cs = (int)__ldcg(H + (int64_t)t * HIST_BINS + (m16 - kap16));
+                if (m16 >= kap16 && m16 - kap16 < (uint32_t)HIST_BINS) cs = (int)Hs[t * HIST_BINS + (m16 - kap16)];
             }
         }
         static_assert(NT >= 64, "segments of a row fit one thread each up to NT");
@@ -991,15 +1017,17 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
             st.flags = FLAG_NONFINITE;
             done = true;
         } else {
+            // (the key-histogram path sums its own, from the histograms)
+            const bool hist_path = sizeof(T) == 2 && p.seg_mode == SEG_HIST && topp_on && !topk_on;
             double s = 0.0;
-            for (int i = threadIdx.x; i < p.nseg; i += NT) {
+            for (int i = threadIdx.x; i < p.nseg && !hist_path; i += NT) {
                 const SegStat* g = p.seg + (int64_t)r * p.nseg + i;
                 const float gm = __ldcg(&g->m);
                 if (gm > -INFINITY)
                     s += __ldcg(&g->s) * exp2(((double)gm - (double)M) * (double)c);
             }
             st.M = M;
-            st.S = block_sum_d(s, s_redd);
+            st.S = hist_path ? 0.0 : block_sum_d(s, s_redd);
             have_stats = true;
             if (!topk_on && !topp_on) done = true;  // MODE_ALL
             if constexpr (sizeof(T) == 2) if (p.seg_mode == SEG_HIST && topp_on && !topk_on) {

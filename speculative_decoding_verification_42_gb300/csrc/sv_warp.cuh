@@ -752,6 +752,199 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
 // k_merge_warp: one warp per row slot (after the stream grid).  The last row //
 // of a sequence to finish (a ticket) decides the sequence.                   //
 // ------------------------------------------------------------------------- //
+// The nucleus (top-p after temperature, no top-k) of bf16 row r by one warp,
+// from the segments' key histograms (SEG_HIST; sv_rows.cu's merge_row_hist
+// does the same with a CTA): each bf16 key's mass is its count times
+// exp2((v - M) c), the tokens below the two-binade window come from the
+// stream's partial sums, and the rank prefix is cut where the mass before a
+// token reaches top_p, ties at the cut key in ascending id (found in the one
+// segment holding the boundary token).  Fills st (MODE_PREFIX, P(x) at the
+// drafted token x) and returns true; false leaves the row to the block merge
+// (a saturated bin, the cut below the window, a nucleus of at most KCAP
+// tokens, which is kept as a list, or more than 32 segments).
+template <typename T>
+__device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, WarpSmem& ws, RowStat& st)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int nseg = p.nseg;
+    static_assert(sizeof(WarpSmem::keys) >= 32 * HIST_BINS, "32 segments' histograms fit the staging");
+    if (nseg > 32) return false;
+    uint8_t* H = reinterpret_cast<uint8_t*>(ws.keys);
+    const SegStat* segs = p.seg + (int64_t)r * nseg;
+    // segment `lane`'s record in this lane, every histogram in shared memory
+    float ms = -INFINITY;
+    double ss = 0.0;
+    if (lane < nseg) {
+        ms = __ldcg(&segs[lane].m);
+        ss = __ldcg(&segs[lane].s);
+    }
+    const uint4* Hg = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.chunk) +
+                                                     (int64_t)r * p.chunk_stride * 2);
+    for (int i = lane; i < nseg * (HIST_BINS / 16); i += 32) reinterpret_cast<uint4*>(H)[i] = __ldcg(Hg + i);
+    const float M = warp_reduce_f(ms, fmax_nan);
+    if (!(M > -INFINITY && M < INFINITY)) {
+        st.flags = FLAG_NONFINITE;
+        return true;
+    }
+    __syncwarp();
+    const uint32_t M16 = key16_bf16(__float_as_uint(M) >> 16);
+    // the tokens below each segment's own window (the stream's sums)
+    double below = (lane < nseg && ms > -INFINITY) ? ss * (double)exp2f((ms - M) * p.c) : 0.0;
+    // lane l holds the row's bins 8 l .. 8 l + 7 (bin d: key M16 - d)
+    uint32_t cnt[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cnt[q] = 0u;
+    bool sat = false;
+    for (int i = 0; i < nseg; ++i) {
+        const float mi = __shfl_sync(FULL, ms, i);
+        if (!(mi > -INFINITY)) continue;
+        const uint32_t m16 = key16_bf16(__float_as_uint(mi) >> 16);
+        const uint32_t off = M16 - m16;  // segment i's window starts off keys below the row's
+        const uint8_t* Hi = H + i * HIST_BINS;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t d = 8u * lane + q;
+            if (d >= off) {
+                const uint32_t c = Hi[d - off];
+                sat |= c == 255u;
+                cnt[q] += c;
+            }
+            if (off + d >= (uint32_t)HIST_BINS) {  // segment bin d lies below the row's window
+                const uint32_t c = Hi[d];
+                sat |= c == 255u;
+                if (c) below += (double)c * (double)hist_weight(p, m16 - d, M);
+            }
+        }
+    }
+    if (__any_sync(FULL, sat)) return false;
+    double mass[8];
+    double lsum = 0.0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t key = M16 - (8u * lane + q);
+        const float w = key >= 0x80u ? hist_weight(p, key, M) : 0.f;
+        mass[q] = (double)cnt[q] * (double)w;
+        lsum += mass[q];
+    }
+    double incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const double S_all = __shfl_sync(FULL, incl, 31) + warp_sum_d(below);
+    const double target = (double)p.top_p * S_all;
+    // the first bin whose inclusive mass reaches the target
+    int cut = -1;
+    double above = 0.0, run = incl - lsum;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        if (cut < 0 && cnt[q] > 0 && run < target && run + mass[q] >= target) {
+            cut = 8 * lane + q;
+            above = run;
+        }
+        run += mass[q];
+    }
+    const unsigned has = __ballot_sync(FULL, cut >= 0);
+    if (!has) return false;  // the cut lies below the window
+    const int src = __ffs(has) - 1;
+    cut = __shfl_sync(FULL, cut, src);
+    above = __shfl_sync(FULL, above, src);
+    int n_lane = 0, cntk = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int d = 8 * lane + q;
+        if (d < cut) n_lane += (int)cnt[q];
+        if (d == cut) cntk = (int)cnt[q];
+    }
+    const int n_above = __reduce_add_sync(FULL, n_lane);
+    cntk = __reduce_add_sync(FULL, cntk);
+    const uint32_t kap16 = M16 - (uint32_t)cut;
+    const float wk = hist_weight(p, kap16, M);
+    int nk = (int)ceil((target - above) / (double)wk);
+    nk = max(1, min(nk, cntk));
+    if (n_above + nk <= KCAP) return false;  // a list: the block merge builds it
+    int32_t ik = p.V - 1;
+    if (nk < cntk) {
+        // the segment holding the nk-th token of key kap16 (in id order)
+        int cs = 0;
+        if (lane < nseg && ms > -INFINITY) {
+            const uint32_t m16 = key16_bf16(__float_as_uint(ms) >> 16);
+            if (m16 >= kap16 && m16 - kap16 < (uint32_t)HIST_BINS) cs = H[lane * HIST_BINS + (m16 - kap16)];
+        }
+        int ci = cs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, ci, o);
+            if (lane >= o) ci += y;
+        }
+        const unsigned hit = __ballot_sync(FULL, ci - cs < nk && nk <= ci);
+        const int sseg = hit ? __ffs(hit) - 1 : 0;
+        const int need = nk - __shfl_sync(FULL, ci - cs, sseg);  // 1-based among the segment's
+        // the segment in id order: lane l walks 256 contiguous tokens, 32
+        // 16-byte words loaded eight at a time
+        constexpr int PER = 256;
+        const unsigned short* rb = reinterpret_cast<const unsigned short*>(row);
+        const int e0 = sseg * (SEG_BYTES / 2) + lane * PER;
+        const int e_end = min(p.V, sseg * (SEG_BYTES / 2) + SEG_BYTES / 2);
+        int mine = 0;
+        for (int w0 = 0; w0 < PER / 8; w0 += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = e0 + (w0 + j) * 8;
+                v[j] = e < e_end ? __ldcg(reinterpret_cast<const uint4*>(rb + e)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t xw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const int e = e0 + (w0 + j) * 8 + h;
+                    const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
+                    mine += (e < e_end && key16_bf16(b16) == kap16) ? 1 : 0;
+                }
+            }
+        }
+        int mi = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, mi, o);
+            if (lane >= o) mi += y;
+        }
+        int found = -1;
+        if (mi - mine < need && need <= mi) {
+            int seen = mi - mine;
+            for (int wd = 0; wd < PER / 8 && found < 0; ++wd) {
+                const int eb = e0 + wd * 8;
+                if (eb >= e_end) break;
+                const uint4 v = __ldcg(reinterpret_cast<const uint4*>(rb + eb));
+                const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+                for (int h = 0; h < 8 && found < 0; ++h) {
+                    const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
+                    if (eb + h < e_end && key16_bf16(b16) == kap16 && ++seen == need) found = eb + h;
+                }
+            }
+        }
+        const unsigned f = __ballot_sync(FULL, found >= 0);
+        if (!f) return false;  // not found (cannot happen with exact counts): the block merge
+        ik = __shfl_sync(FULL, found, __ffs(f) - 1);
+    }
+    st.M = M;
+    st.S = above + (double)nk * (double)wk;
+    st.mode = MODE_PREFIX;
+    st.kappa = key_of(val_key16(kap16));
+    st.i_kappa = ik;
+    st.n_kept = n_above + nk;
+    st.flags = 0;
+    if (x >= 0) {
+        const float lx = Elem<T>::load_cg(row, x);
+        st.px = kept_prefix(st, key_of(lx), x) ? row_prob(p, lx, M, st.S) : 0.f;
+    }
+    return true;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
 {
@@ -792,6 +985,10 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     st.pad[0] = st.pad[1] = st.pad[2] = 0;
     if (p.seg_mode == SEG_CHUNK) {
         if (!warp_fast_topk<T>(p, row, r, x, ws, st)) st.flags |= FLAG_BLOCK_MERGE;
+    } else if (p.seg_mode == SEG_HIST) {
+        bool ok = false;
+        if constexpr (sizeof(T) == 2) ok = warp_hist_nucleus<T>(p, row, r, x, ws, st);
+        if (!ok) st.flags |= FLAG_BLOCK_MERGE;
     } else {
         warp_all_stats(p, r, st);
         if (!st.flags && x >= 0) st.px = row_prob(p, Elem<T>::load_cg(row, x), st.M, st.S);
