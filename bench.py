@@ -52,14 +52,10 @@ def _tensor_peak():
 
 
 def _stage1_kernel(w) -> str:
-    """The kernel that streams the logits for this workload's knobs: the
-    fused top-k kernel for top-k rows on 16 bytes (1 <= k <= 128), else the
-    stream kernel (rows on 16 bytes) or the per-segment kernel."""
+    """The kernel that streams the logits for this workload's knobs."""
     row_bytes = w.V * (2 if w.dtype == "bf16" else 4)
     if row_bytes % 16:
         return "k_rows"
-    if w.temperature > 0 and 1 <= w.top_k <= 128 and w.top_k < w.V and w.draft_kind == "logits":
-        return "k_verify_topk"
     return "k_stream"
 
 

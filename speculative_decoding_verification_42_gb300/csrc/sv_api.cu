@@ -37,7 +37,6 @@ struct spec_verify {
     unsigned* err;
     unsigned* seq_done;
     unsigned* exit_flag;  // early exit: a sequence was left to the regular pipeline
-    unsigned* work_ctr;   // [2] the fused kernel's work counter and exit ticket
     // spec_verify_set_profiling: events around the stage-1 stream kernel and
     // where each run stores the number of kernels it launched (all optional)
     cudaEvent_t prof_begin;
@@ -45,9 +44,6 @@ struct spec_verify {
     int32_t* prof_launches;
     float* logits;        // the LM head's output (SPEC_TARGET_HIDDEN_LMHEAD), else NULL
     int fault;            // spec_verify_inject_fault: the fault armed for the next run
-    // chunk keys may be left nonzero by a launch other than the fused top-k
-    // kernel (which needs them at 0 when it starts): clear them before it
-    bool keys_dirty;
     // where the workspace came from (NULL: cudaMalloc / cudaFree)
     spec_alloc_fn alloc_fn;
     spec_release_fn release_fn;
@@ -134,7 +130,6 @@ void fill_workspace(const spec_verify* h, Params& p)
     p.chunk_stride = h->chunk_stride;
     p.err = h->err;
     p.seq_done = h->seq_done;
-    p.work_ctr = h->work_ctr;
 }
 
 // one workspace: 256-byte aligned sub-buffers for max_batch x max_k x vocab.
@@ -180,7 +175,6 @@ size_t layout_workspace(spec_verify* h, void* base)
     const size_t o_err = take(sizeof(unsigned));
     const size_t o_sd = take(sizeof(unsigned) * cfg->max_batch);
     const size_t o_xf = take(sizeof(unsigned));
-    const size_t o_wc = take(2 * sizeof(unsigned));
     const bool lmhead = cfg->target_kind == SPEC_TARGET_HIDDEN_LMHEAD;
     const size_t o_logits =
         lmhead ? take(sizeof(float) * (size_t)cfg->max_batch * (cfg->max_k + 1) * (size_t)V) : 0;
@@ -201,7 +195,6 @@ size_t layout_workspace(spec_verify* h, void* base)
         h->err = (unsigned*)(b + o_err);
         h->seq_done = (unsigned*)(b + o_sd);
         h->exit_flag = (unsigned*)(b + o_xf);
-        h->work_ctr = (unsigned*)(b + o_wc);
         h->logits = lmhead ? (float*)(b + o_logits) : nullptr;
     }
     return off;
@@ -210,28 +203,11 @@ size_t layout_workspace(spec_verify* h, void* base)
 // stage 1: stream every row (the persistent bulk-copy kernel when every row
 // starts on a 16-byte boundary, else one CTA per segment); then merge the rows
 // (one warp per row when the knobs allow, else one CTA per row) and decide the
-// sequences, each grid a programmatic dependent launch of the one before.
-// Top-k rows on 16 bytes take the fused kernel instead (stream and row merges
-// in one grid), then the decision grid.
+// sequences, each grid a programmatic dependent launch of the one before
 cudaError_t launch_stage1(spec_verify* h, Params& p, int dtype, bool vec, cudaStream_t s, int* launches,
-                          bool timed = true, bool allow_fused = true)
+                          bool timed = true)
 {
     const bool rec = timed && h->prof_begin;
-    if (allow_fused && p.cand && vec) {
-        if (h->keys_dirty) {
-            const size_t kb = sizeof(uint16_t) * (size_t)h->chunk_stride * (size_t)p.B * (size_t)p.rps;
-            if (cudaMemsetAsync(h->chunk, 0, kb, s) != cudaSuccess) return cudaErrorUnknown;
-            h->keys_dirty = false;
-        }
-        p.fused = 1;
-        if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
-        cudaError_t e = launch_verify_topk(p, dtype, h->num_sms, s);
-        if (e != cudaSuccess) return e;
-        if (rec && cudaEventRecord(h->prof_end, s) != cudaSuccess) return cudaErrorUnknown;
-        *launches += 2;
-        return launch_decide(p, dtype, s);
-    }
-    if (p.seg_mode != SEG_SUM) h->keys_dirty = true;  // chunk keys or key histograms
     if (rec && cudaEventRecord(h->prof_begin, s) != cudaSuccess) return cudaErrorUnknown;
     cudaError_t e = vec ? launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, s)
                         : launch_rows(p, dtype, false, s);
@@ -425,7 +401,6 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
         h->fault = SPEC_FAULT_NONE;
         p.stall = 1;
         p.wait_limit = STALL_WAIT_POLLS;
-        if (p.seg_mode != SEG_SUM) h->keys_dirty = true;
         if (launch_rows_stream(p, dtype, STREAM_CTAS_PER_SM * h->num_sms, cs) != cudaSuccess)
             return SPEC_ERR_CUDA;
         if (h->prof_launches) *h->prof_launches = 1;
@@ -453,7 +428,6 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
     // it returns at once unless that kernel raised the flag
     const bool exit = early_exit && p.cand && !lmhead;
     if (exit) {
-        h->keys_dirty = true;  // the early-exit kernel writes chunk keys
         p.exit_flag = h->exit_flag;
         if (cudaMemsetAsync(h->exit_flag, 0, sizeof(unsigned), cs) != cudaSuccess) return SPEC_ERR_CUDA;
         if (h->prof_begin && cudaEventRecord(h->prof_begin, cs) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -465,7 +439,7 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
         // the row merge (softmax partials of the LM head) and the decision grid
         launches += 2;
         if (launch_merge_warp(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
-    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead && !exit, !exit) != cudaSuccess) {
+    } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead && !exit) != cudaSuccess) {
         return SPEC_ERR_CUDA;
     }
     if (!all_lists(p)) {
@@ -579,12 +553,10 @@ spec_status spec_verify_check(spec_verify_t h, void* stream)
         cudaMemsetAsync(h->seq_ticket, 0, sizeof(unsigned) * (size_t)h->cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h->seq_done, 0, sizeof(unsigned) * (size_t)h->cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h->job_ticket, 0, sizeof(unsigned) * (size_t)h->jobs_cap, cs) != cudaSuccess ||
-        cudaMemsetAsync(h->work_ctr, 0, 2 * sizeof(unsigned), cs) != cudaSuccess ||
         cudaStreamSynchronize(cs) != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
     }
-    h->keys_dirty = true;
     return SPEC_ERR_TIMEOUT;
 }
 
@@ -678,7 +650,6 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
     const size_t need = layout_over(&h, cfg, in->batch, in->k_max, ws, ws_bytes);
     if (need == 0 || need > ws_bytes) return SPEC_ERR_INVALID_ARG;
     h.num_sms = num_sms;
-    h.keys_dirty = true;  // the array keeps whatever the last call left in its chunk keys
     // the counters the kernels expect at zero (the array keeps the last call's contents)
     cudaStream_t cs = (cudaStream_t)stream;
     const size_t tickets = sizeof(unsigned) * (size_t)h.rows_cap;
@@ -686,8 +657,7 @@ spec_status sv_noalloc_run(void* ws, size_t ws_bytes, int num_sms, const spec_ve
         cudaMemsetAsync(h.seq_ticket, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
         cudaMemsetAsync(h.job_ticket, 0, sizeof(unsigned) * (size_t)h.jobs_cap, cs) != cudaSuccess ||
         cudaMemsetAsync(h.err, 0, sizeof(unsigned), cs) != cudaSuccess ||
-        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess ||
-        cudaMemsetAsync(h.work_ctr, 0, 2 * sizeof(unsigned), cs) != cudaSuccess)
+        cudaMemsetAsync(h.seq_done, 0, sizeof(unsigned) * (size_t)h.cfg.max_batch, cs) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return spec_verify_run(&h, in, s, out, stream);
 }

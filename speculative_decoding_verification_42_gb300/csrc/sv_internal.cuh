@@ -152,11 +152,6 @@ struct Params {
     // wait_limit polls; 0 / 0 in every ordinary run
     int32_t stall;
     uint32_t wait_limit;      // 0: WAIT_LIMIT
-    // 1: the top-k rows run the fused kernel (sv_fused.cuh), which takes a 0
-    // chunk key for a chunk not streamed yet; whoever reads a row's keys last
-    // writes 0 back
-    int32_t fused;
-    unsigned* work_ctr;       // [2]: the fused kernel's next work item, producers done (0 between launches)
 };
 
 constexpr int CAND_TOPK_MAX = 128;  // largest top-k the row merge of sv_mcand.cuh serves
@@ -619,10 +614,6 @@ cudaError_t launch_rows_stream(const Params& p, int dtype, int ctas, cudaStream_
 // top-k rows: the row merge (one CTA per row) and the decision grid for what
 // it leaves, both programmatic dependents of the stream
 cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s);
-// top-k rows as one persistent kernel (stream and row merges at once,
-// cooperative launch), then the decision grid for what it leaves
-cudaError_t launch_verify_topk(const Params& p, int dtype, int num_sms, cudaStream_t s);
-cudaError_t launch_decide(const Params& p, int dtype, cudaStream_t s);
 // early-exit verify of the top-k rows (one CTA per sequence at a time)
 cudaError_t launch_verify_exit(const Params& p, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_merge(const Params& p, int dtype, cudaStream_t s);

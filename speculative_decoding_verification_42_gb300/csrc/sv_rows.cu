@@ -174,9 +174,7 @@ __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int se
     const int64_t base = (int64_t)seg * G::SEG;
     if constexpr (MODE == SEG_CHUNK) {
         // 8 consecutive lanes hold one 128-byte chunk: its NaN-propagating max
-        // becomes a 16-bit order key (a lower bound of every key in the chunk).
-        // Key 0 is kept free (keys up to 0x7F all mean "no finite logit"): the
-        // fused top-k kernel takes a 0 for a chunk not streamed yet
+        // becomes a 16-bit order key (a lower bound of every key in the chunk)
         typename CM::P m[G::ROUNDS];
 #pragma unroll
         for (int i = 0; i < G::ROUNDS; ++i) m[i] = CM::lane(fetch(i));
@@ -191,7 +189,7 @@ __device__ __forceinline__ void segment_compute(const Params& p, F fetch, int se
                 const int64_t e0 = base + ((int64_t)i * NTH + lt) * G::VW;
                 if (e0 < V)
                     p.chunk[(int64_t)r * p.chunk_stride + e0 / G::CHUNK_EL] =
-                        (uint16_t)max(key_of(CM::value(m[i])) >> 16, 1u);
+                        (uint16_t)(key_of(CM::value(m[i])) >> 16);
             }
         }
     } else if constexpr (MODE == SEG_HIST) {
@@ -487,6 +485,70 @@ __device__ int collect_prefix(const T* row, int V, const RowStat& fin, float M, 
     }
     *S_out = block_sum_d((double)s, s_red_d);
     return offset;
+}
+
+template <typename T> __device__ __forceinline__ float word_elem(uint4 w, int q);
+
+// The same for a row on 16 bytes: each thread walks a contiguous range of
+// 16-byte words (eight in flight at a time), counting its kept tokens and
+// summing them; one block scan gives every thread its offset in the list, and
+// a second walk (from L2) writes the tokens in ascending id.
+template <typename T>
+__device__ int collect_prefix_vec(const T* row, int V, const RowStat& fin, float M, float c, int32_t* kid,
+                                  float* kl, double* S_out)
+{
+    __shared__ int s_red_i[NT / 32 + 1];
+    __shared__ double s_red_d[NT / 32 + 1];
+    constexpr int VW = Vec16<T>::N;
+    const int nw = V / VW;
+    const int per = (nw + NT - 1) / NT;
+    const int w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    int cnt = 0;
+    float s = 0.f;
+    for (int w = w0; w < w1; w += 8) {
+        uint4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = w + j < w1 ? __ldcg(rv + w + j) : Vec16<T>::neg_inf();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int q = 0; q < VW; ++q) {
+                const float l = word_elem<T>(x[j], q);
+                if (w + j < w1 && kept_prefix(fin, key_of(l), (w + j) * VW + q)) {
+                    ++cnt;
+                    s += ex2_fast((l - M) * c);
+                }
+            }
+    }
+    int total;
+    int off = block_excl_scan<int>(cnt, s_red_i, &total);
+    *S_out = block_sum_d((double)s, s_red_d);
+    if (total <= KCAP && cnt > 0) {
+        for (int w = w0; w < w1; ++w) {
+            const uint4 x = __ldcg(rv + w);
+#pragma unroll
+            for (int q = 0; q < VW; ++q) {
+                const float l = word_elem<T>(x, q);
+                if (kept_prefix(fin, key_of(l), w * VW + q)) {
+                    kid[off] = w * VW + q;
+                    kl[off] = l;
+                    ++off;
+                }
+            }
+        }
+    }
+    return total;
+}
+
+// the kept list of a rank prefix by whichever walk the row's alignment allows
+template <typename T>
+__device__ int collect_kept(const T* row, int V, const RowStat& fin, float M, float c, int32_t* kid, float* kl,
+                            double* S_out)
+{
+    if (((uintptr_t)row & 15u) == 0 && ((int64_t)V * (int64_t)sizeof(T)) % 16 == 0)
+        return collect_prefix_vec<T>(row, V, fin, M, c, kid, kl, S_out);
+    return collect_prefix<T>(row, V, fin, M, c, kid, kl, S_out);
 }
 
 // ------------------------------------------------------------------------- //
@@ -1037,7 +1099,7 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
                 if (h == 0) {
                     if (st.n_kept <= KCAP) {  // a small nucleus becomes a list (one pass)
                         double S;
-                        const int nk = collect_prefix<T>(row, V, st, st.M, c, kid, kl, &S);
+                        const int nk = collect_kept<T>(row, V, st, st.M, c, kid, kl, &S);
                         st.S = S;
                         st.n_kept = nk;
                         st.mode = MODE_LIST;
@@ -1078,7 +1140,7 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
                     pre.kappa = kap;
                     pre.i_kappa = ik;
                 }
-                if (topp_on) collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S_pre);
+                if (topp_on) collect_kept<T>(row, V, pre, st.M, c, kid, kl, &S_pre);
             }
             if (topp_on) {
                 SelCfg cfg;
@@ -1097,7 +1159,7 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
                 }
             }
             double S;
-            const int nk = collect_prefix<T>(row, V, pre, st.M, c, kid, kl, &S);
+            const int nk = collect_kept<T>(row, V, pre, st.M, c, kid, kl, &S);
             st.S = S;
             st.n_kept = nk;
             st.kappa = pre.kappa;
@@ -1567,6 +1629,88 @@ struct Ring {
 };
 constexpr int STREAM_SMEM = NSTAGE * SEG_BYTES;
 
+// One warp reduces a whole segment (SEG_SUM, SEG_HIST): no barrier with the
+// other warps, so each of the CTA's stream warps keeps its own segment in
+// flight.  Two reads of the segment in shared memory: its max M, then the sum
+// of exp2((l - M) c) (SEG_HIST: over the tokens more than HIST_BINS keys below
+// M, and a count per key for the others, in the warp's own histogram).
+template <typename T, int MODE>
+__device__ __forceinline__ void warp_segment(const Params& p, const uint4* sv4, int seg, int r, uint32_t* hist)
+{
+    constexpr int VW = Vec16<T>::N;
+    constexpr int SEGE = SEG_BYTES / (int)sizeof(T);
+    constexpr int WPL = SEGE / VW / 32;  // 16-byte words per lane
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int64_t base = (int64_t)seg * SEGE;
+    const int nvalid = (int)min((int64_t)SEGE, (int64_t)p.V - base);  // tokens of the segment
+    auto word = [&](int i) {
+        const int q = i * 32 + lane;
+        return q * VW < nvalid ? sv4[q] : Vec16<T>::neg_inf();
+    };
+    float m = -INFINITY;
+#pragma unroll 8
+    for (int i = 0; i < WPL; ++i) m = fmax_nan(m, Vec16<T>::vmax(word(i)));
+    const float M = warp_reduce_f(m, fmax_nan);
+    float s = 0.f;
+    if (M > -INFINITY && M < INFINITY) {
+        const float c = p.c, Mc = M * p.c;
+        if constexpr (MODE == SEG_HIST) {
+            const uint32_t m16 = key16_bf16(__float_as_uint(M) >> 16);
+            const uint32_t lo16 = m16 >= 0x7Fu + (HIST_BINS - 1) ? m16 - (HIST_BINS - 1) : 0x7Fu;
+            const uint32_t thr = __float_as_uint(val_key16(lo16)) >> 16;
+            const uint32_t thr2 = thr | (thr << 16);
+            float sh[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums: shorter rounding chains
+#pragma unroll 4
+            for (int i = 0; i < WPL; ++i) {
+                const uint4 w = word(i);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t x = ws[h];
+                    const uint32_t in = ChunkMax<__nv_bfloat16>::ge2(x, thr2);  // 0xFFFF per counted half
+                    const float elo = ex2_fast(fmaf(bf16_lo(x), c, -Mc));
+                    const float ehi = ex2_fast(fmaf(bf16_hi(x), c, -Mc));
+                    sh[h] += ((in & 0xFFFFu) ? 0.f : elo) + ((in >> 16) ? 0.f : ehi);
+                    if (in & 0xFFFFu) atomicAdd(&hist[m16 - key16_bf16(x & 0xFFFFu)], 1u);
+                    if (in >> 16) atomicAdd(&hist[m16 - key16_bf16(x >> 16)], 1u);
+                }
+            }
+            s = (sh[0] + sh[1]) + (sh[2] + sh[3]);
+        } else {
+            float sh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int i = 0; i < WPL; ++i) sh[i & 3] += Vec16<T>::vsumexp(word(i), M, c);
+            s = (sh[0] + sh[1]) + (sh[2] + sh[3]);
+        }
+    }
+    s = warp_reduce_f(s, [](float a, float b) { return a + b; });
+    if constexpr (MODE == SEG_HIST) {
+        __syncwarp();
+        // the counts out, four u8 bins per word (saturating), and cleared
+        uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.chunk) +
+                                                    (int64_t)r * p.chunk_stride * 2 + (int64_t)seg * HIST_BINS);
+#pragma unroll
+        for (int q = lane; q < HIST_BINS / 4; q += 32) {
+            uint32_t wd = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                wd |= min(hist[4 * q + j], 255u) << (8 * j);
+                hist[4 * q + j] = 0u;
+            }
+            out[q] = wd;
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {
+        SegStat st;
+        st.m = M;
+        st.pad = 0.f;
+        st.s = (double)s;
+        p.seg[(int64_t)r * p.nseg + seg] = st;
+    }
+}
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
 {
@@ -1575,11 +1719,17 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     __shared__ Ring ring;
     __shared__ float s_redf[NS / 32 + 1];
     __shared__ double s_redd[NS / 32 + 1];
-    __shared__ uint32_t s_hist[MODE == SEG_HIST ? HIST_BINS : 1];
+    // SEG_SUM and SEG_HIST: each stream warp reduces whole segments on its own
+    // (stage k belongs to warp k mod NSTAGE); SEG_CHUNK: the four warps share
+    // every segment
+    constexpr bool PERWARP = MODE != SEG_CHUNK;
+    constexpr int NSENT = PERWARP ? NS / 32 : 1;  // end-of-work sentinels
+    static_assert(!PERWARP || NSTAGE == NS / 32, "one stage per stream warp");
+    __shared__ uint32_t s_hist[MODE == SEG_HIST ? (NS / 32) * HIST_BINS : 1];
     using G = SegGeom<T, NS>;
     const int tid = threadIdx.x;
     if (MODE == SEG_HIST)
-        for (int i = tid; i < HIST_BINS; i += STREAM_THREADS) s_hist[i] = 0u;
+        for (int i = tid; i < (NS / 32) * HIST_BINS; i += STREAM_THREADS) s_hist[i] = 0u;
     // the merge kernel that follows may be scheduled as this grid drains; it
     // waits for this grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1618,7 +1768,18 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
             }
             ring.item[s] = (int)item;
             if (item < 0) {
-                mbar_arrive(&ring.full[s]);  // the end-of-work sentinel
+                // the end-of-work sentinel, one per consumer (the next NSENT stages)
+                mbar_arrive(&ring.full[s]);
+                for (int g = 1; g < NSENT; ++g) {
+                    ++k;
+                    const int s2 = k % NSTAGE;
+                    if (k >= NSTAGE && !mbar_wait(&ring.empty[s2], ((k / NSTAGE) - 1) & 1)) {
+                        atomicOr(p.err, 1u);
+                        break;
+                    }
+                    ring.item[s2] = -1;
+                    mbar_arrive(&ring.full[s2]);
+                }
                 break;
             }
             const int r = (int)(item / p.nseg), seg = (int)(item - (int64_t)r * p.nseg);
@@ -1635,6 +1796,27 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
             // wait (bounded) for the copies still in flight before leaving
             for (int q = (k > NSTAGE ? k - NSTAGE : 0); q < k; ++q)
                 mbar_wait(&ring.full[q % NSTAGE], (q / NSTAGE) & 1);
+        }
+        return;
+    }
+
+    if constexpr (PERWARP) {
+        // ---------------- stream warps, one segment each at a time
+        const unsigned FULL = 0xffffffffu;
+        const int w = tid >> 5;
+        for (int k = w;; k += NS / 32) {
+            const int s = k % NSTAGE;
+            if (!__all_sync(FULL, mbar_wait_n(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
+                if ((tid & 31) == 0) atomicOr(p.err, 2u);
+                break;
+            }
+            const int item = ring.item[s];
+            if (item < 0) break;
+            const int r = item / p.nseg, seg = item - r * p.nseg;
+            warp_segment<T, MODE>(p, reinterpret_cast<const uint4*>(smem_ring + (size_t)s * SEG_BYTES), seg, r,
+                                  s_hist + (MODE == SEG_HIST ? w * HIST_BINS : 0));
+            __syncwarp();  // every lane is done with the stage
+            if ((tid & 31) == 0) mbar_arrive(&ring.empty[s]);
         }
         return;
     }
@@ -1689,7 +1871,6 @@ __global__ void __launch_bounds__(NT, 4) k_merge(const Params p)
 #include "sv_warp.cuh"
 #include "sv_mcand.cuh"
 #include "sv_exit.cuh"
-#include "sv_fused.cuh"
 
 namespace sv {
 
@@ -1766,18 +1947,6 @@ static cudaError_t launch_merge_topk_t(const Params& p, cudaStream_t s)
     cudaError_t e = launch_dependent(k_merge_cand<T>, p, (unsigned)(p.B * p.rps), MC_T, 0, s);
     if (e != cudaSuccess) return e;
     return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
-}
-
-cudaError_t launch_verify_topk(const Params& p, int dtype, int num_sms, cudaStream_t s)
-{
-    return dtype == 1 ? launch_verify_topk_t<__nv_bfloat16>(p, num_sms, s)
-                      : launch_verify_topk_t<float>(p, num_sms, s);
-}
-
-cudaError_t launch_decide(const Params& p, int dtype, cudaStream_t s)
-{
-    return dtype == 1 ? launch_dependent(k_decide<__nv_bfloat16>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s)
-                      : launch_dependent(k_decide<float>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
 }
 
 cudaError_t launch_merge_topk(const Params& p, int dtype, cudaStream_t s)

@@ -1055,11 +1055,6 @@ __global__ void __launch_bounds__(NT) k_decide(const Params p)
         const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
         merge_row<T>(p, row, r, smem_scratch);
         csync();
-        if (p.fused) {
-            // the fused kernel left this row's chunk keys for this merge: 0 them
-            uint4* k = reinterpret_cast<uint4*>(p.chunk + (int64_t)r * p.chunk_stride);
-            for (int w = threadIdx.x; w < p.chunk_stride / 8; w += NT) __stcg(k + w, make_uint4(0, 0, 0, 0));
-        }
         merged = true;
     }
     if (merged) {

@@ -440,12 +440,11 @@ def test_draft_sampler_parity(orc, V, dtype, knobs):
             np.testing.assert_allclose(probs[b, j], P, rtol=1e-5, atol=1e-9)
 
 
-def test_fused_topk_handle_reuse(orc):
-    """The fused top-k kernel takes a 0 chunk key for a chunk not streamed yet.
-    On one handle, its runs interleaved with launches that leave chunk keys
-    behind (the draft-side sampler, the early-exit verify, a tie-heavy batch
-    whose rows go to the block merge of the decision grid) all match the
-    oracle."""
+def test_handle_reuse_across_paths(orc):
+    """One handle serving, in turn, the verify of top-k rows, the draft-side
+    sampler, the early-exit verify and a tie-heavy batch whose rows go to the
+    block merge of the decision grid: every verify matches the oracle (no run
+    depends on what an earlier one left in the workspace)."""
     import torch
     import speculative_decoding_verification_42_gb300 as sv
     from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
@@ -458,8 +457,8 @@ def test_fused_topk_handle_reuse(orc):
     toks = {id(w): oracle_tokens(orc, w)[0], id(wt): oracle_tokens(orc, wt)[0]}
     ver = sv.Verifier(vocab=w.V, max_batch=w.B, max_k=w.K_max, dtype="bf16")
     kpr = torch.from_numpy(w.k_per_row).cuda()
-    plan = [("fused", w), ("draft", w), ("fused", w), ("exit", w), ("fused", wt), ("fused", w),
-            ("fused", wt), ("fused", w)]
+    plan = [("verify", w), ("draft", w), ("verify", w), ("exit", w), ("verify", wt), ("verify", w),
+            ("verify", wt), ("verify", w)]
     for kind, wk in plan:
         if kind == "draft":
             ver.draft_sample(to_device(wk.draft), kpr, temperature=wk.temperature,
