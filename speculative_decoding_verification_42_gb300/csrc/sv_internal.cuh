@@ -143,6 +143,7 @@ struct Params {
     unsigned long long* job_part; // [njobs, nseg_sample, SAMPLE_PARTS] the segments' round masses
     unsigned* job_ticket;     // [njobs]
     int32_t nseg_sample;      // stage-2 segments per row
+    int32_t sample_spc;       // stage-2 segments per CTA (set by the launcher)
     unsigned* err;            // bounded waits that ran out (0 = none)
     int32_t cand;             // 1: top-k rows (1 <= top-k <= CAND_TOPK_MAX) take k_merge_cand
     unsigned* exit_flag;      // early exit: the regular pipeline runs only when it is nonzero (NULL: always)

@@ -489,65 +489,74 @@ __device__ int collect_prefix(const T* row, int V, const RowStat& fin, float M, 
 
 template <typename T> __device__ __forceinline__ float word_elem(uint4 w, int q);
 
-// The same for a row on 16 bytes: each thread walks a contiguous range of
-// 16-byte words (eight in flight at a time), counting its kept tokens and
-// summing them; one block scan gives every thread its offset in the list, and
-// a second walk (from L2) writes the tokens in ascending id.
+// The same for a row on 16 bytes, in one pass: coalesced rounds of LPT
+// 16-byte words per thread in flight; every kept token goes to a staging
+// list in shared memory (an atomic slot, id << 32 | logit bits) while the
+// thread sums its mass; when the prefix has at most KCAP tokens the staging
+// is sorted by id (bitonic) and written out as the ordered list.
+constexpr int COLLECT_STAGE_OFF = 24576;  // staging offset in a merge's scratch (after the radix bins)
 template <typename T>
 __device__ int collect_prefix_vec(const T* row, int V, const RowStat& fin, float M, float c, int32_t* kid,
-                                  float* kl, double* S_out)
+                                  float* kl, double* S_out, unsigned long long* stage)
 {
-    __shared__ int s_red_i[NT / 32 + 1];
+    __shared__ int s_n;
     __shared__ double s_red_d[NT / 32 + 1];
     constexpr int VW = Vec16<T>::N;
+    constexpr int LPT = 16;
     const int nw = V / VW;
-    const int per = (nw + NT - 1) / NT;
-    const int w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
     const uint4* rv = reinterpret_cast<const uint4*>(row);
-    int cnt = 0;
+    if (threadIdx.x == 0) s_n = 0;
+    csync();
     float s = 0.f;
-    for (int w = w0; w < w1; w += 8) {
-        uint4 x[8];
+    for (int w0 = 0; w0 < nw; w0 += NT * LPT) {
+        uint4 x[LPT];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = w + j < w1 ? __ldcg(rv + w + j) : Vec16<T>::neg_inf();
+        for (int j = 0; j < LPT; ++j) {
+            const int w = w0 + j * NT + (int)threadIdx.x;
+            x[j] = w < nw ? __ldcg(rv + w) : Vec16<T>::neg_inf();
+        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < LPT; ++j) {
+            const int w = w0 + j * NT + (int)threadIdx.x;
 #pragma unroll
             for (int q = 0; q < VW; ++q) {
                 const float l = word_elem<T>(x[j], q);
-                if (w + j < w1 && kept_prefix(fin, key_of(l), (w + j) * VW + q)) {
-                    ++cnt;
+                const int e = w * VW + q;
+                if (w < nw && kept_prefix(fin, key_of(l), e)) {
                     s += ex2_fast((l - M) * c);
-                }
-            }
-    }
-    int total;
-    int off = block_excl_scan<int>(cnt, s_red_i, &total);
-    *S_out = block_sum_d((double)s, s_red_d);
-    if (total <= KCAP && cnt > 0) {
-        for (int w = w0; w < w1; ++w) {
-            const uint4 x = __ldcg(rv + w);
-#pragma unroll
-            for (int q = 0; q < VW; ++q) {
-                const float l = word_elem<T>(x, q);
-                if (kept_prefix(fin, key_of(l), w * VW + q)) {
-                    kid[off] = w * VW + q;
-                    kl[off] = l;
-                    ++off;
+                    const int pos = atomicAdd(&s_n, 1);
+                    if (pos < KCAP) stage[pos] = ((unsigned long long)(uint32_t)e << 32) | __float_as_uint(l);
                 }
             }
         }
     }
+    csync();
+    const int total = s_n;
+    *S_out = block_sum_d((double)s, s_red_d);
+    if (total <= KCAP) {
+        const int n2 = next_pow2(total);
+        for (int i = total + (int)threadIdx.x; i < n2; i += NT) stage[i] = ~0ull;
+        csync();
+        bitonic_sort_u64(stage, n2);
+        for (int i = threadIdx.x; i < total; i += NT) {
+            kid[i] = (int32_t)(stage[i] >> 32);
+            kl[i] = __uint_as_float((uint32_t)stage[i]);
+        }
+    }
+    csync();  // the staging may be reused
     return total;
 }
 
 // the kept list of a rank prefix by whichever walk the row's alignment allows
 template <typename T>
 __device__ int collect_kept(const T* row, int V, const RowStat& fin, float M, float c, int32_t* kid, float* kl,
-                            double* S_out)
+                            double* S_out, unsigned char* scratch)
 {
+    static_assert(COLLECT_STAGE_OFF + KCAP * 8 <= SCRATCH_BYTES && NBINS * 8 <= COLLECT_STAGE_OFF,
+                  "the staging fits the scratch after the radix bins");
     if (((uintptr_t)row & 15u) == 0 && ((int64_t)V * (int64_t)sizeof(T)) % 16 == 0)
-        return collect_prefix_vec<T>(row, V, fin, M, c, kid, kl, S_out);
+        return collect_prefix_vec<T>(row, V, fin, M, c, kid, kl, S_out,
+                                     reinterpret_cast<unsigned long long*>(scratch + COLLECT_STAGE_OFF));
     return collect_prefix<T>(row, V, fin, M, c, kid, kl, S_out);
 }
 
@@ -613,7 +622,6 @@ __device__ bool fast_topk(const Params& p, const T* row, int r, unsigned char* s
 {
     __shared__ int s_cnt, s_nqual, s_flag, s_nk;
     __shared__ int s_red_i[NT / 32 + 1];
-    __shared__ double s_redd[NT / 32 + 1];
     unsigned long long* srt = (unsigned long long*)(scratch + SC_CK);   // sorted, CAND_CAP
     unsigned long long* cand = (unsigned long long*)(scratch + SC_CAND);
     int32_t* qual = (int32_t*)(scratch + SC_QUAL);
@@ -1008,24 +1016,43 @@ __device__ int merge_row_hist(const Params& p, const T* row, int r, RowStat& st,
         const int e_begin = sseg * G::SEG;
         const int e_end = min(p.V, e_begin + G::SEG);
         constexpr int EPT = G::SEG / NT;  // contiguous elements per thread
+        constexpr int WPT = EPT / 8;      // their 16-byte words, loaded in one round
+        static_assert(EPT % 8 == 0, "a thread's tokens are whole words");
         const int e0 = e_begin + t * EPT;
+        uint4 wv[WPT];
+#pragma unroll
+        for (int j = 0; j < WPT; ++j)
+            wv[j] = e0 + 8 * j < e_end ? __ldcg(reinterpret_cast<const uint4*>((const unsigned short*)row + e0 + 8 * j))
+                                       : make_uint4(0, 0, 0, 0);
+        // bit 8 j + h: token e0 + 8 j + h has key kap16 (a row on 16 bytes
+        // holds whole words up to e_end)
+        uint32_t hit[WPT];
         int mine = 0;
-        for (int i = 0; i < EPT; ++i) {
-            const int e = e0 + i;
-            if (e < e_end && key16_bf16((uint32_t)__ldcg((const unsigned short*)row + e)) == kap16) ++mine;
+#pragma unroll
+        for (int j = 0; j < WPT; ++j) {
+            const uint32_t xw[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+            hit[j] = 0u;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
+                if (e0 + 8 * j + h < e_end && key16_bf16(b16) == kap16) hit[j] |= 1u << h;
+            }
+            mine += __popc(hit[j]);
         }
         const int mb = block_excl_scan<int>(mine, s_redi, &dummy);
         if (t == 0) s_id = p.V - 1;
         csync();
         if (mb < need && need <= mb + mine) {
             int seen = mb;
-            for (int i = 0; i < EPT; ++i) {
-                const int e = e0 + i;
-                if (e < e_end && key16_bf16((uint32_t)__ldcg((const unsigned short*)row + e)) == kap16 &&
-                    ++seen == need) {
-                    s_id = e;
+#pragma unroll
+            for (int j = 0; j < WPT; ++j) {
+                if (seen + __popc(hit[j]) >= need) {
+                    uint32_t m = hit[j];
+                    for (int q = 0; q < need - seen - 1; ++q) m &= m - 1u;  // drop the earlier hits
+                    s_id = e0 + 8 * j + __ffs(m) - 1;
                     break;
                 }
+                seen += __popc(hit[j]);
             }
         }
         csync();
@@ -1099,7 +1126,7 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
                 if (h == 0) {
                     if (st.n_kept <= KCAP) {  // a small nucleus becomes a list (one pass)
                         double S;
-                        const int nk = collect_kept<T>(row, V, st, st.M, c, kid, kl, &S);
+                        const int nk = collect_kept<T>(row, V, st, st.M, c, kid, kl, &S, scratch);
                         st.S = S;
                         st.n_kept = nk;
                         st.mode = MODE_LIST;
@@ -1140,7 +1167,7 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
                     pre.kappa = kap;
                     pre.i_kappa = ik;
                 }
-                if (topp_on) collect_kept<T>(row, V, pre, st.M, c, kid, kl, &S_pre);
+                if (topp_on) collect_kept<T>(row, V, pre, st.M, c, kid, kl, &S_pre, scratch);
             }
             if (topp_on) {
                 SelCfg cfg;
@@ -1159,7 +1186,7 @@ __device__ void merge_row(const Params& p, const T* row, int r, unsigned char* s
                 }
             }
             double S;
-            const int nk = collect_kept<T>(row, V, pre, st.M, c, kid, kl, &S);
+            const int nk = collect_kept<T>(row, V, pre, st.M, c, kid, kl, &S, scratch);
             st.S = S;
             st.n_kept = nk;
             st.kappa = pre.kappa;
@@ -1629,6 +1656,74 @@ struct Ring {
 };
 constexpr int STREAM_SMEM = NSTAGE * SEG_BYTES;
 
+// paired fp32 arithmetic (two lanes of a 64-bit register per instruction)
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float f2_sum(unsigned long long r)
+{
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+    return a + b;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// SEG_HIST for a segment whose window [val(lo16), M] holds positive values
+// only: per token, exp2((l - M) c) is summed when l is below the window
+// (exp2 of -inf adds 0 for the others) and its count is added to bin
+// m16 - key = (m16 - 0x8000) - bits when it is inside (a positive bf16's key
+// is its bits + 0x8000); -inf padding is below the window and adds 0.
+template <bool FULLSEG>
+__device__ __forceinline__ float warp_hist_pos(const uint4* sv4, int nvalid, int lane, float c, float Mc,
+                                               uint32_t m16, uint32_t lo16, uint32_t* hist)
+{
+    constexpr int SEGE = SEG_BYTES / 2;
+    constexpr int WPL = SEGE / 8 / 32;
+    const float thrf = val_key16(lo16);
+    const unsigned long long c2 = f2_pack(c, c), nmc2 = f2_pack(-Mc, -Mc);
+    const uint32_t hb = smem_u32(hist) + 4u * (m16 - 0x8000u);  // hb - 4 h: the bin of bits h
+    unsigned long long s2[2] = {0ull, 0ull};  // four running sums, in two pairs
+    // (the counts need no memory clobber: the stage is only read here, and the
+    // warp's __syncwarp orders them before the histogram is read out)
+#pragma unroll 4
+    for (int i = 0; i < WPL; ++i) {
+        const int q = i * 32 + lane;
+        const uint4 w = (FULLSEG || q * 8 < nvalid) ? sv4[q] : Vec16<__nv_bfloat16>::neg_inf();
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint32_t x = ws[h];
+            const float lo = bf16_lo(x), hi = bf16_hi(x);
+            const bool inlo = lo >= thrf, inhi = hi >= thrf;
+            float alo, ahi;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(alo), "=f"(ahi) : "l"(f2_fma(f2_pack(lo, hi), c2, nmc2)));
+            const float elo = ex2_fast(inlo ? -INFINITY : alo);
+            const float ehi = ex2_fast(inhi ? -INFINITY : ahi);
+            s2[h >> 1] = f2_add(s2[h >> 1], f2_pack(elo, ehi));
+            asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}"
+                         ::"r"(hb - ((x & 0xFFFFu) << 2)), "r"((uint32_t)inlo));
+            asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}"
+                         ::"r"(hb - ((x >> 16) << 2)), "r"((uint32_t)inhi));
+        }
+    }
+    return f2_sum(s2[0]) + f2_sum(s2[1]);
+}
+
 // One warp reduces a whole segment (SEG_SUM, SEG_HIST): no barrier with the
 // other warps, so each of the CTA's stream warps keeps its own segment in
 // flight.  Two reads of the segment in shared memory: its max M, then the sum
@@ -1640,7 +1735,6 @@ __device__ __forceinline__ void warp_segment(const Params& p, const uint4* sv4, 
     constexpr int VW = Vec16<T>::N;
     constexpr int SEGE = SEG_BYTES / (int)sizeof(T);
     constexpr int WPL = SEGE / VW / 32;  // 16-byte words per lane
-    const unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     const int64_t base = (int64_t)seg * SEGE;
     const int nvalid = (int)min((int64_t)SEGE, (int64_t)p.V - base);  // tokens of the segment
@@ -1658,25 +1752,32 @@ __device__ __forceinline__ void warp_segment(const Params& p, const uint4* sv4, 
         if constexpr (MODE == SEG_HIST) {
             const uint32_t m16 = key16_bf16(__float_as_uint(M) >> 16);
             const uint32_t lo16 = m16 >= 0x7Fu + (HIST_BINS - 1) ? m16 - (HIST_BINS - 1) : 0x7Fu;
-            const uint32_t thr = __float_as_uint(val_key16(lo16)) >> 16;
-            const uint32_t thr2 = thr | (thr << 16);
-            float sh[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums: shorter rounding chains
+            if (lo16 > 0x8000u) {
+                // the window holds positive values only: a token's bin is
+                // (m16 - 0x8000) - its bf16 bits
+                if (nvalid == SEGE) s = warp_hist_pos<true>(sv4, nvalid, lane, c, Mc, m16, lo16, hist);
+                else s = warp_hist_pos<false>(sv4, nvalid, lane, c, Mc, m16, lo16, hist);
+            } else {
+                const uint32_t thr = __float_as_uint(val_key16(lo16)) >> 16;
+                const uint32_t thr2 = thr | (thr << 16);
+                float sh[4] = {0.f, 0.f, 0.f, 0.f};  // four running sums: shorter rounding chains
 #pragma unroll 4
-            for (int i = 0; i < WPL; ++i) {
-                const uint4 w = word(i);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                for (int i = 0; i < WPL; ++i) {
+                    const uint4 w = word(i);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint32_t x = ws[h];
-                    const uint32_t in = ChunkMax<__nv_bfloat16>::ge2(x, thr2);  // 0xFFFF per counted half
-                    const float elo = ex2_fast(fmaf(bf16_lo(x), c, -Mc));
-                    const float ehi = ex2_fast(fmaf(bf16_hi(x), c, -Mc));
-                    sh[h] += ((in & 0xFFFFu) ? 0.f : elo) + ((in >> 16) ? 0.f : ehi);
-                    if (in & 0xFFFFu) atomicAdd(&hist[m16 - key16_bf16(x & 0xFFFFu)], 1u);
-                    if (in >> 16) atomicAdd(&hist[m16 - key16_bf16(x >> 16)], 1u);
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t x = ws[h];
+                        const uint32_t in = ChunkMax<__nv_bfloat16>::ge2(x, thr2);  // 0xFFFF per counted half
+                        const float elo = ex2_fast(fmaf(bf16_lo(x), c, -Mc));
+                        const float ehi = ex2_fast(fmaf(bf16_hi(x), c, -Mc));
+                        sh[h] += ((in & 0xFFFFu) ? 0.f : elo) + ((in >> 16) ? 0.f : ehi);
+                        if (in & 0xFFFFu) atomicAdd(&hist[m16 - key16_bf16(x & 0xFFFFu)], 1u);
+                        if (in >> 16) atomicAdd(&hist[m16 - key16_bf16(x >> 16)], 1u);
+                    }
                 }
+                s = (sh[0] + sh[1]) + (sh[2] + sh[3]);
             }
-            s = (sh[0] + sh[1]) + (sh[2] + sh[3]);
         } else {
             float sh[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -1736,7 +1837,8 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&ring.full[s], 1);
-            mbar_init(&ring.empty[s], 1);
+            // SEG_CHUNK: each of the four warps releases the stage on its own
+            mbar_init(&ring.empty[s], PERWARP ? 1 : NS / 32);
         }
         fence_barrier_init();
     }
@@ -1755,8 +1857,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
             if (item >= total_items) {
                 item = -1;
             } else {
-                const int r = (int)(item / p.nseg), seg = (int)(item - (int64_t)r * p.nseg);
-                const RowRef rr = row_ref(p, r);
+                const RowRef rr = row_ref(p, (int)(item / p.nseg));
                 if (!rr.valid) continue;
                 if (rr.is_draft && !drafts_streamed(p)) continue;
             }
@@ -1818,30 +1919,33 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
             __syncwarp();  // every lane is done with the stage
             if ((tid & 31) == 0) mbar_arrive(&ring.empty[s]);
         }
-        return;
-    }
-
-    // ---------------- stream threads
-    for (int k = 0;; ++k) {
-        const int s = k % NSTAGE;
-        if (!ssync_and(mbar_wait_n(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
-            if (tid == 0) atomicOr(p.err, 2u);
-            break;
+    } else {
+        // ---------------- stream threads (SEG_CHUNK): the four warps share each
+        // segment but need no barrier among them: a chunk's key is one lane group's
+        // own, and every warp waits for, and releases, the stage by itself (so a
+        // wait that runs out ends one warp without stranding the others)
+        static_assert(PERWARP || MODE == SEG_CHUNK, "the shared-segment loop has no barriers");
+        for (int k = 0;; ++k) {
+            const int s = k % NSTAGE;
+            if (!__all_sync(0xffffffffu, mbar_wait_n(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
+                if ((tid & 31) == 0) atomicOr(p.err, 2u);
+                break;
+            }
+            const int item = ring.item[s];
+            if (item < 0) break;
+            const int r = item / p.nseg, seg = item - r * p.nseg;
+            const uint4* sv4 = reinterpret_cast<const uint4*>(smem_ring + (size_t)s * SEG_BYTES);
+            const int64_t base = (int64_t)seg * G::SEG;
+            segment_compute<T, MODE, NS>(
+                p,
+                [&](int i) {
+                    const int64_t e0 = base + ((int64_t)i * NS + tid) * G::VW;
+                    return e0 < p.V ? sv4[i * NS + tid] : Vec16<T>::neg_inf();
+                },
+                seg, r, tid, [] {}, s_redf, s_redd, s_hist);
+            __syncwarp();  // the warp is done with the stage
+            if ((tid & 31) == 0) mbar_arrive(&ring.empty[s]);
         }
-        const int item = ring.item[s];
-        if (item < 0) break;
-        const int r = item / p.nseg, seg = item - r * p.nseg;
-        const uint4* sv4 = reinterpret_cast<const uint4*>(smem_ring + (size_t)s * SEG_BYTES);
-        const int64_t base = (int64_t)seg * G::SEG;
-        segment_compute<T, MODE, NS>(
-            p,
-            [&](int i) {
-                const int64_t e0 = base + ((int64_t)i * NS + tid) * G::VW;
-                return e0 < p.V ? sv4[i * NS + tid] : Vec16<T>::neg_inf();
-            },
-            seg, r, tid, [] { ssync(); }, s_redf, s_redd, s_hist);
-        ssync();  // every stream thread is done with the stage
-        if (tid == 0) mbar_arrive(&ring.empty[s]);
     }
 }
 

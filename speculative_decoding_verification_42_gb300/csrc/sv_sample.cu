@@ -9,6 +9,8 @@
 // id: the smallest v with C(v) > u Z.  Masses are summed exactly as 2^-56
 // fixed-point integers so the per-segment totals, the prefix over segments and
 // the rescan of the crossing segment agree bit for bit.
+#include <algorithm>
+
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -102,6 +104,7 @@ __device__ __forceinline__ unsigned long long dense_r_fix(const DenseJob& J, flo
 {
     const float pt = dense_pt(J, c, l, v);
     if (!J.residual) return to_fix56(pt);
+    if (!(pt > 0.f)) return 0ull;  // max(0, 0 - p_d) = 0: the draft need not be read
     float pd;
     if (J.dkind == 1) {
         pd = d;
@@ -199,7 +202,7 @@ __device__ unsigned long long segment_pass(const DenseJob& J, float c, int V, in
         for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
         if (lane == 0) s_part[q * (NT / 32) + warp] = w;
     }
-    __syncthreads();
+    csync();
     unsigned long long total = 0;
     if (threadIdx.x < G::SQ) {
         unsigned long long r = 0;
@@ -207,41 +210,36 @@ __device__ unsigned long long segment_pass(const DenseJob& J, float c, int V, in
         parts[threadIdx.x] = r;
         s_red[threadIdx.x] = r;
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0)
         for (int q = 0; q < G::SQ; ++q) total += s_red[q];
-    __syncthreads();  // s_part and s_red may be reused
+    csync();  // s_part and s_red may be reused
     return total;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
-{
-    if (exit_skip(p)) return;
-    using G = SampleGeom<T>;
-    __shared__ unsigned long long s_red[NT / 32 + 1];
-    __shared__ unsigned long long s_part[4 * (NT / 32)];
-    __shared__ unsigned long long s_base;
-    __shared__ int s_last, s_star, s_tok;
-    const int V = p.V, nseg = p.nseg_sample;
-    const int jid = blockIdx.x / nseg, seg = blockIdx.x - jid * nseg;
-    const Job jb = load_job(p.jobs + jid);
-    if (jb.kind == JOB_NONE) return;
-    const bool residual = jb.kind == JOB_RESIDUAL;
-    DenseJob J = make_job<T>(p, jb, residual);
-    unsigned long long* parts = p.job_part + (int64_t)jid * nseg * SAMPLE_PARTS;
+// the scratch of a sampling CTA
+struct SampleSmem {
+    unsigned long long red[NT / 32 + 1];
+    unsigned long long part[4 * (NT / 32)];
+    unsigned long long base;
+    int last, star, tok;
+};
 
-    const unsigned long long zs =
-        segment_pass<T>(J, p.c, V, seg, parts + (int64_t)seg * SAMPLE_PARTS, s_part, s_red);
-    if (threadIdx.x == 0) {
-        p.job_seg[(int64_t)jid * nseg + seg] = zs;
-        __threadfence();  // the segment's masses are visible before its ticket
-        s_last = atomicAdd(&p.job_ticket[jid], 1u) == (unsigned)(nseg - 1);
-        if (s_last) __threadfence();
-    }
-    __syncthreads();
-    if (!s_last) return;
-    // ---- the last segment of the job: locate u Z, segment -> part -> element
+// the sample of job jid once every segment of it is summed (job_seg, job_part
+// complete and visible), by every thread of the CTA: locate u Z, segment ->
+// round -> element; the residual that summed to 0 falls back to p_t itself
+template <typename T>
+__device__ void sample_tail(const Params& p, int jid, const Job& jb, DenseJob J, SampleSmem& sm)
+{
+    using G = SampleGeom<T>;
+    const int V = p.V, nseg = p.nseg_sample;
+    const bool residual = jb.kind == JOB_RESIDUAL;
+    unsigned long long* parts = p.job_part + (int64_t)jid * nseg * SAMPLE_PARTS;
+    unsigned long long* s_red = sm.red;
+    unsigned long long* s_part = sm.part;
+    unsigned long long& s_base = sm.base;
+    int& s_star = sm.star;
+    int& s_tok = sm.tok;
     if (threadIdx.x == 0) {
         p.job_ticket[jid] = 0u;
         s_tok = -1;
@@ -260,7 +258,7 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
                 if (threadIdx.x == 0) seg_tot[sg] = z;
             }
             __threadfence_block();
-            __syncthreads();
+            csync();
         }
         const unsigned long long z = threadIdx.x < nseg ? __ldcg(seg_tot + threadIdx.x) : 0ull;
         unsigned long long Z;
@@ -272,12 +270,12 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
         }
         const unsigned long long t = cdf_target(jb.u, Z);
         if (threadIdx.x == 0) s_star = -1;
-        __syncthreads();
+        csync();
         if (threadIdx.x < nseg && exs <= t && t < exs + z) {
             s_star = threadIdx.x;
             s_base = exs;
         }
-        __syncthreads();
+        csync();
         const int star = s_star;
         if (star < 0) break;  // no segment holds u Z (cannot happen when Z > 0)
         // the round of the crossing segment holding u Z (thread 0, in order)
@@ -294,7 +292,7 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
             }
             s_base = acc;  // the mass before that round
         }
-        __syncthreads();
+        csync();
         const int qs = s_star;
         // that round again, one word per thread, then the thread and element
         const int v0 = word_at<T>(star * SAMPLE_SEG, qs);
@@ -322,7 +320,7 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
                 }
             }
         }
-        __syncthreads();
+        csync();
         break;
     }
     if (threadIdx.x == 0) {
@@ -332,6 +330,285 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
             if (zero && p.row_status) p.row_status[jb.b] = ROW_ZERO_RESIDUAL;
         }
         p.jobs[jid].kind = JOB_NONE;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
+{
+    if (exit_skip(p)) return;
+    __shared__ SampleSmem sm;
+    const int V = p.V, nseg = p.nseg_sample;
+    // CTA c of a job takes the segments [c spc, (c + 1) spc)
+    const int spc = p.sample_spc > 0 ? p.sample_spc : 1;
+    const int nct = (nseg + spc - 1) / spc;
+    const int jid = blockIdx.x / nct, cta = blockIdx.x - jid * nct;
+    const Job jb = load_job(p.jobs + jid);
+    if (jb.kind == JOB_NONE) return;
+    const bool residual = jb.kind == JOB_RESIDUAL;
+    DenseJob J = make_job<T>(p, jb, residual);
+    unsigned long long* parts = p.job_part + (int64_t)jid * nseg * SAMPLE_PARTS;
+
+    for (int seg = cta * spc; seg < min(nseg, (cta + 1) * spc); ++seg) {
+        const unsigned long long zs =
+            segment_pass<T>(J, p.c, V, seg, parts + (int64_t)seg * SAMPLE_PARTS, sm.part, sm.red);
+        if (threadIdx.x == 0) p.job_seg[(int64_t)jid * nseg + seg] = zs;
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();  // the segments' masses are visible before the ticket
+        sm.last = atomicAdd(&p.job_ticket[jid], 1u) == (unsigned)(nct - 1);
+        if (sm.last) __threadfence();
+    }
+    __syncthreads();
+    if (!sm.last) return;
+    sample_tail<T>(p, jid, jb, J, sm);
+}
+
+// ------------------------------------------------------------------------- //
+// k_sample_ring: the same sums and sample for rows on 16 bytes, by a          //
+// persistent grid that streams the jobs' segments through shared memory.     //
+// Item i (job i / nseg, segment i % nseg) goes to CTA i mod gridDim; thread 0 //
+// keeps up to SR_STAGES items in flight as bulk copies (the target segment,  //
+// the draft segment when the residual reads the draft densely), each landing //
+// on the stage's mbarrier; every thread then sums its words of the stage in  //
+// the same fixed point and rounds as segment_pass.  The CTA that sums a      //
+// job's last segment (a ticket) draws the job's sample (sample_tail).        //
+// ------------------------------------------------------------------------- //
+constexpr int SR_STAGES = 4;
+
+// bytes of one stage: the target segment, then the draft segment
+__host__ __device__ constexpr int sr_stage_bytes(int tsize, int dsize) { return SAMPLE_SEG * (tsize + dsize); }
+// stages of the ring: 64 KB of them (two to SR_STAGES), so that three CTAs
+// share an SM for every row type
+__host__ __device__ constexpr int sr_stages(int stage_bytes)
+{
+    return 65536 / stage_bytes < 2 ? 2 : 65536 / stage_bytes > SR_STAGES ? SR_STAGES : 65536 / stage_bytes;
+}
+
+// the job's draft is read densely (a residual against draft logits not kept
+// as a list, or draft probabilities)
+__device__ __forceinline__ bool draft_dense(const DenseJob& J)
+{
+    return J.residual && (J.dkind == 1 || J.ds.mode != MODE_LIST);
+}
+
+// SW consecutive elements of a staged segment (element index i of the
+// segment) into out, fill beyond n valid elements
+template <typename U, int SW>
+__device__ __forceinline__ void stage_word(const unsigned char* st, int i, int n, float fill, float* out)
+{
+    if (i + SW <= n) {
+        constexpr int NV = SW * (int)sizeof(U) / 16;
+#pragma unroll
+        for (int g = 0; g < NV; ++g) {
+            const uint4 w = reinterpret_cast<const uint4*>(st + (size_t)i * sizeof(U))[g];
+            const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+            if (sizeof(U) == 4) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) out[g * 4 + k] = __uint_as_float(x[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    out[g * 8 + 2 * k] = bf16_lo(x[k]);
+                    out[g * 8 + 2 * k + 1] = bf16_hi(x[k]);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < SW; ++e) {
+            if (i + e < n) {
+                if (sizeof(U) == 4) out[e] = reinterpret_cast<const float*>(st)[i + e];
+                else out[e] = __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(st)[i + e] << 16);
+            } else {
+                out[e] = fill;
+            }
+        }
+    }
+}
+
+constexpr int SR_THREADS = NT + 32;  // NT sampling threads, then the copy warp
+
+// csync() returning whether v held in every sampling thread
+__device__ __forceinline__ bool csync_and(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+                 "bar.red.and.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)v), "n"(NT) : "memory");
+    return r != 0;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, int njobs)
+{
+    if (exit_skip(p)) return;
+    using G = SampleGeom<T>;
+    extern __shared__ __align__(128) unsigned char sr_ring[];
+    __shared__ SampleSmem sm;
+    __shared__ uint64_t s_full[SR_STAGES], s_empty[SR_STAGES];
+    __shared__ int s_item[SR_STAGES];
+    __shared__ Job s_jb[SR_STAGES];
+    __shared__ DenseJob s_job[SR_STAGES];
+    const int V = p.V, nseg = p.nseg_sample;
+    const int dsize = p.draft_kind == 1 ? 4 : (int)sizeof(T);
+    const int stage_bytes = sr_stage_bytes((int)sizeof(T), dsize);
+    const int NST = sr_stages(stage_bytes);  // stages in the ring
+    const int64_t n_items = (int64_t)njobs * nseg;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], NT / 32);  // each sampling warp frees the stage
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();  // the only barrier over all SR_THREADS threads
+
+    if (tid >= NT) {
+        // ---------------- the copy warp (one thread): the CTA's items in
+        // order, each job's record and rows resolved here and handed over
+        // with the stage
+        if (tid != NT) return;
+        const uint64_t pol = l2_evict_first();
+        int k = 0;
+        for (int64_t i = blockIdx.x;; i += gridDim.x) {
+            int jid = -1;
+            Job jb;
+            if (i < n_items) {
+                jid = (int)(i / nseg);
+                jb = load_job(p.jobs + jid);
+                if (jb.kind == JOB_NONE) continue;
+            }
+            const int s = k % NST;
+            if (k >= NST && !mbar_wait(&s_empty[s], ((k / NST) - 1) & 1)) {
+                atomicOr(p.err, 4u);
+                // wait (bounded) for the copies still in flight before leaving
+                for (int q = (k > NST ? k - NST : 0); q < k; ++q) mbar_wait(&s_full[q % NST], (q / NST) & 1);
+                return;
+            }
+            if (jid < 0) {
+                s_item[s] = -1;  // the end: one marker ends every sampling thread
+                mbar_arrive(&s_full[s]);
+                return;
+            }
+            const int seg = (int)(i - (int64_t)jid * nseg);
+            const DenseJob J = make_job<T>(p, jb, jb.kind == JOB_RESIDUAL);
+            s_item[s] = (int)i;
+            s_jb[s] = jb;
+            s_job[s] = J;
+            const int n = min(SAMPLE_SEG, V - seg * SAMPLE_SEG);
+            const uint32_t tb = (uint32_t)n * (uint32_t)sizeof(T);
+            const uint32_t db = draft_dense(J) ? (uint32_t)n * (uint32_t)dsize : 0u;
+            unsigned char* dst = sr_ring + (size_t)s * stage_bytes;
+            mbar_arrive_expect_tx(&s_full[s], tb + db);  // releases the records above
+            tma_load_1d_once(dst, (const T*)J.trow + (int64_t)seg * SAMPLE_SEG, tb, &s_full[s], pol);
+            if (db)
+                tma_load_1d_once(dst + SAMPLE_SEG * sizeof(T),
+                                 (const char*)J.drow + (int64_t)seg * SAMPLE_SEG * dsize, db, &s_full[s], pol);
+            ++k;
+        }
+    }
+
+    // ---------------- the sampling threads
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int k = 0;; ++k) {
+        const int s = k % NST;
+        if (!csync_and(mbar_wait_n(&s_full[s], (k / NST) & 1, p.wait_limit))) {
+            if (tid == 0) atomicOr(p.err, 4u);
+            break;
+        }
+        const int item = s_item[s];
+        if (item < 0) break;
+        const int jid = item / nseg, seg = item - jid * nseg;
+        const Job jb = s_jb[s];
+        DenseJob J = s_job[s];
+        const unsigned char* st = sr_ring + (size_t)s * stage_bytes;
+        const unsigned char* sd = st + SAMPLE_SEG * sizeof(T);
+        const int n = min(SAMPLE_SEG, V - seg * SAMPLE_SEG);
+        const int base = seg * SAMPLE_SEG;
+        // this thread's words of the stage, one round at a time (word q:
+        // elements (q NT + tid) SW ..)
+        const bool dd = draft_dense(J);
+        unsigned long long wm[G::SQ];
+        int dptr = 0;
+        if (J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST)
+            dptr = lower_bound_i32(J.dids, J.ds.n_kept, min(base + tid * G::SW, V));
+#pragma unroll
+        for (int q = 0; q < G::SQ; ++q) {
+            const int i = (q * NT + tid) * G::SW;
+            const int v0 = base + i;
+            float lt[G::SW], dv[G::SW];
+            stage_word<T, G::SW>(st, i, n, -INFINITY, lt);
+            if (!dd) {
+#pragma unroll
+                for (int e = 0; e < G::SW; ++e) dv[e] = 0.f;
+            } else if (J.dkind == 1) {
+                stage_word<float, G::SW>(sd, i, n, 0.f, dv);
+            } else {
+                stage_word<T, G::SW>(sd, i, n, -INFINITY, dv);
+            }
+            wm[q] = 0ull;
+            if (J.ts.mode == MODE_ALL) {
+                // every token of the target is kept
+#pragma unroll
+                for (int e = 0; e < G::SW; ++e)
+                    if (v0 + e < V) wm[q] += dense_r_fix(J, p.c, lt[e], dv[e], v0 + e, dptr);
+            } else {
+                // R(v) = 0 wherever p_t(v) = 0 (outside the target's kept
+                // rank prefix): a mask of the word's kept tokens first, then
+                // the mass of those alone, in ascending v, so that a row with
+                // few kept tokens costs the warp a few passes, not one per token
+                uint32_t km = 0u;
+#pragma unroll
+                for (int e = 0; e < G::SW; ++e)
+                    if (v0 + e < V && kept_prefix(J.ts, key_of(lt[e]), v0 + e)) km |= 1u << e;
+                while (km) {
+                    const int b = __ffs(km) - 1;
+                    km &= km - 1u;
+                    float l = 0.f, d = 0.f;  // element b, picked without indexing the arrays
+#pragma unroll
+                    for (int e = 0; e < G::SW; ++e)
+                        if (e == b) {
+                            l = lt[e];
+                            d = dv[e];
+                        }
+                    wm[q] += dense_r_fix(J, p.c, l, d, v0 + b, dptr);
+                }
+            }
+        }
+        __syncwarp();  // the warp is done with the stage
+        if (lane == 0) mbar_arrive(&s_empty[s]);
+        // per round, then the segment, then its ticket
+        unsigned long long* parts = p.job_part + ((int64_t)jid * nseg + seg) * SAMPLE_PARTS;
+#pragma unroll
+        for (int q = 0; q < G::SQ; ++q) {
+            unsigned long long w = wm[q];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+            if (lane == 0) sm.part[q * (NT / 32) + warp] = w;
+        }
+        csync();
+        if (tid < G::SQ) {
+            unsigned long long r = 0;
+            for (int i = 0; i < NT / 32; ++i) r += sm.part[tid * (NT / 32) + i];
+            parts[tid] = r;
+            sm.red[tid] = r;
+        }
+        csync();
+        if (tid == 0) {
+            unsigned long long zs = 0;
+            for (int q = 0; q < G::SQ; ++q) zs += sm.red[q];
+            p.job_seg[(int64_t)jid * nseg + seg] = zs;
+            __threadfence();  // the segment's masses are visible before its ticket
+            sm.last = atomicAdd(&p.job_ticket[jid], 1u) == (unsigned)(nseg - 1);
+            if (sm.last) __threadfence();
+        }
+        csync();
+        if (sm.last) {
+            sample_tail<T>(p, jid, jb, J, sm);
+            csync();  // sm is free again
+        }
     }
 }
 
@@ -450,12 +727,60 @@ cudaError_t launch_alpha(const Params& p, int dtype, cudaStream_t s)
     return cudaGetLastError();
 }
 
+// every row the samplers may read starts on 16 bytes and holds whole
+// 16-byte words (the bulk copies of the ring kernel need both)
+static bool rows_on_16(const Params& p, int dtype)
+{
+    const int64_t ts = dtype == 1 ? 2 : 4;
+    if (((int64_t)p.V * ts) % 16 != 0 || ((int64_t)p.V * 4) % 16 != 0) return false;
+    const void* t = p.draft_launch ? p.draft : p.target;
+    return ((uintptr_t)t & 15u) == 0 && ((uintptr_t)p.draft & 15u) == 0;
+}
+
+template <typename T>
+static cudaError_t launch_sample_ring(const Params& p, int njobs, cudaStream_t s)
+{
+    const int dsize = p.draft_kind == 1 ? 4 : (int)sizeof(T);
+    const int smem = sr_stages(sr_stage_bytes((int)sizeof(T), dsize)) * sr_stage_bytes((int)sizeof(T), dsize);
+    struct Geo {
+        int sms, per_sm;
+    };
+    static DeviceOnce once[2];  // per device and draft kind: the opt-in and the CTAs per SM
+    Geo g{0, 0};
+    int packed = 0;
+    const cudaError_t e = cuda_once(once[p.draft_kind == 1], &packed, [smem](int dev, int* out) {
+        cudaError_t r = cudaFuncSetAttribute(k_sample_ring<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        int sms = 0, per = 0;
+        if (r == cudaSuccess) r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_sample_ring<T>, SR_THREADS, smem);
+        *out = sms * 16 + (per < 1 ? 1 : per > 15 ? 15 : per);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
+    g.sms = packed / 16;
+    g.per_sm = packed % 16;
+    const int64_t items = (int64_t)njobs * p.nseg_sample;
+    const int grid = (int)std::min<int64_t>(items, (int64_t)g.sms * g.per_sm);
+    k_sample_ring<T><<<grid, SR_THREADS, smem, s>>>(p, njobs);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s)
 {
     if (njobs <= 0 || p.nseg_sample <= 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((int64_t)njobs * p.nseg_sample);
-    if (dtype == 1) k_sample<__nv_bfloat16><<<grid, NT, 0, s>>>(p);
-    else k_sample<float><<<grid, NT, 0, s>>>(p);
+    if (rows_on_16(p, dtype))
+        return dtype == 1 ? launch_sample_ring<__nv_bfloat16>(p, njobs, s) : launch_sample_ring<float>(p, njobs, s);
+    // rows off 16 bytes: one CTA per (job, group of segments), about eight
+    // CTAs per SM in all
+    Params q = p;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t segs = (int64_t)njobs * p.nseg_sample;
+    q.sample_spc = (int)std::max<int64_t>(1, (segs + 8LL * sms - 1) / (8LL * sms));
+    const int nct = (p.nseg_sample + q.sample_spc - 1) / q.sample_spc;
+    const unsigned grid = (unsigned)((int64_t)njobs * nct);
+    if (dtype == 1) k_sample<__nv_bfloat16><<<grid, NT, 0, s>>>(q);
+    else k_sample<float><<<grid, NT, 0, s>>>(q);
     return cudaGetLastError();
 }
 

@@ -888,24 +888,38 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
         const unsigned short* rb = reinterpret_cast<const unsigned short*>(row);
         const int e0 = sseg * (SEG_BYTES / 2) + lane * PER;
         const int e_end = min(p.V, sseg * (SEG_BYTES / 2) + SEG_BYTES / 2);
-        int mine = 0;
-        for (int w0 = 0; w0 < PER / 8; w0 += 8) {
+        // the lane's hits of key kap16, one 8-bit mask per word of the
+        // current group, counted per group of eight words
+        constexpr int NG = PER / 64;  // groups of eight words
+        auto group_hits = [&](int g, uint32_t (&hm)[8]) {
             uint4 v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int e = e0 + (w0 + j) * 8;
+                const int e = e0 + (8 * g + j) * 8;
                 v[j] = e < e_end ? __ldcg(reinterpret_cast<const uint4*>(rb + e)) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t xw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                hm[j] = 0u;
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
-                    const int e = e0 + (w0 + j) * 8 + h;
+                    const int e = e0 + (8 * g + j) * 8 + h;
                     const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
-                    mine += (e < e_end && key16_bf16(b16) == kap16) ? 1 : 0;
+                    if (e < e_end && key16_bf16(b16) == kap16) hm[j] |= 1u << h;
                 }
             }
+        };
+        int gc[NG];
+        int mine = 0;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            uint32_t hm[8];
+            group_hits(g, hm);
+            gc[g] = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gc[g] += __popc(hm[j]);
+            mine += gc[g];
         }
         int mi = mine;
 #pragma unroll
@@ -915,16 +929,19 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
         }
         int found = -1;
         if (mi - mine < need && need <= mi) {
-            int seen = mi - mine;
-            for (int wd = 0; wd < PER / 8 && found < 0; ++wd) {
-                const int eb = e0 + wd * 8;
-                if (eb >= e_end) break;
-                const uint4 v = __ldcg(reinterpret_cast<const uint4*>(rb + eb));
-                const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
-                for (int h = 0; h < 8 && found < 0; ++h) {
-                    const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
-                    if (eb + h < e_end && key16_bf16(b16) == kap16 && ++seen == need) found = eb + h;
+            // the group holding it, re-read (one round from L2), then the word
+            int seen = mi - mine, g = 0;
+            while (g < NG - 1 && seen + gc[g] < need) seen += gc[g++];
+            uint32_t hm[8];
+            group_hits(g, hm);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (found < 0 && seen + __popc(hm[j]) >= need) {
+                    uint32_t m = hm[j];
+                    for (int q = 0; q < need - seen - 1; ++q) m &= m - 1u;  // drop the earlier hits
+                    found = e0 + (8 * g + j) * 8 + __ffs(m) - 1;
                 }
+                seen += __popc(hm[j]);
             }
         }
         const unsigned f = __ballot_sync(FULL, found >= 0);
