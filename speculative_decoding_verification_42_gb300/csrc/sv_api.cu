@@ -442,10 +442,7 @@ spec_status run_verify(spec_verify_t h, const spec_verify_inputs* in, const spec
     } else if (launch_stage1(h, p, dtype, vec, cs, &launches, !lmhead && !exit) != cudaSuccess) {
         return SPEC_ERR_CUDA;
     }
-    if (!all_lists(p)) {
-        if (launch_sample(p, dtype, p.B, cs) != cudaSuccess) return SPEC_ERR_CUDA;
-        ++launches;
-    }
+    if (!all_lists(p) && launch_sample(p, dtype, p.B, cs, &launches) != cudaSuccess) return SPEC_ERR_CUDA;
     if (p.alpha) {
         if (launch_alpha(p, dtype, cs) != cudaSuccess) return SPEC_ERR_CUDA;
         ++launches;

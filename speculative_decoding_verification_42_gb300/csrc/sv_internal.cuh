@@ -645,7 +645,7 @@ __host__ __device__ __forceinline__ bool warp_merge_ok(const Params& p)
                                (p.seg_mode == SEG_SUM && p.top_k == 0 && !(p.top_p < 1.0f)) ||
                                (p.seg_mode == SEG_HIST && p.top_k == 0 && p.nseg <= 32));
 }
-cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s);
+cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s, int* launches = nullptr);
 // alpha_j = sum_v min(p_t, p_d) of every slot (when p.alpha is set)
 cudaError_t launch_alpha(const Params& p, int dtype, cudaStream_t s);
 // the LM head: out[M, N] (row stride ldo) = hidden[M, K] x w[K, N], bf16 in, fp32 out

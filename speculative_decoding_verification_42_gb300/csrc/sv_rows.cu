@@ -882,8 +882,9 @@ __device__ __forceinline__ float hist_weight(const Params& p, uint32_t k, float 
     if (!(d > -INFINITY)) return 0.f;
     const float x = d * p.c;
     const float x_lo = fmaf(d, p.c, -x) + d * p.c_lo;  // the rounding of d c, and d c_lo
-    const float n = rintf(x);
-    return ldexpf(exp2f((x - n) + x_lo), (int)n);
+    const float n = rintf(x);  // <= 0: v <= M
+    if (n < -126.f) return 0.f;  // below 2^-126 of the max token's: no mass at fp32 range
+    return exp2f((x - n) + x_lo) * __int_as_float(((int)n + 127) << 23);  // an exact power-of-two scale
 }
 
 // Finds the nucleus (top-p after temperature, no top-k) of row r from the
@@ -2040,7 +2041,7 @@ static cudaError_t launch_merge_warp_t(const Params& p, cudaStream_t s)
     });
     if (e0 != cudaSuccess) return e0;
     cudaError_t e = launch_dependent(k_merge_warp<T>, p, (unsigned)((rows + WM_WARPS - 1) / WM_WARPS),
-                                     WM_WARPS * 32, WM_SMEM, s);
+                                     WM_WARPS * 32, WM_WARPS * wm_stride(p.seg_mode), s);
     if (e != cudaSuccess) return e;
     return launch_dependent(k_decide<T>, p, (unsigned)p.B, NT, SCRATCH_BYTES, s);
 }

@@ -371,8 +371,10 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
 // keeps up to SR_STAGES items in flight as bulk copies (the target segment,  //
 // the draft segment when the residual reads the draft densely), each landing //
 // on the stage's mbarrier; every thread then sums its words of the stage in  //
-// the same fixed point and rounds as segment_pass.  The CTA that sums a      //
-// job's last segment (a ticket) draws the job's sample (sample_tail).        //
+// the same fixed point and rounds as segment_pass.  The samples are drawn    //
+// by k_sample_tail, one CTA per job, after the whole grid: a CTA that drew   //
+// them as it summed a job's last segment fell behind the others and kept     //
+// summing last segments (and drawing) for the rest of the grid.              //
 // ------------------------------------------------------------------------- //
 constexpr int SR_STAGES = 4;
 
@@ -579,7 +581,8 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
         }
         __syncwarp();  // the warp is done with the stage
         if (lane == 0) mbar_arrive(&s_empty[s]);
-        // per round, then the segment, then its ticket
+        // per round, then the segment (the samples are drawn by the next
+        // grid, k_sample_tail, once every segment is summed)
         unsigned long long* parts = p.job_part + ((int64_t)jid * nseg + seg) * SAMPLE_PARTS;
 #pragma unroll
         for (int q = 0; q < G::SQ; ++q) {
@@ -600,16 +603,22 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
             unsigned long long zs = 0;
             for (int q = 0; q < G::SQ; ++q) zs += sm.red[q];
             p.job_seg[(int64_t)jid * nseg + seg] = zs;
-            __threadfence();  // the segment's masses are visible before its ticket
-            sm.last = atomicAdd(&p.job_ticket[jid], 1u) == (unsigned)(nseg - 1);
-            if (sm.last) __threadfence();
         }
-        csync();
-        if (sm.last) {
-            sample_tail<T>(p, jid, jb, J, sm);
-            csync();  // sm is free again
-        }
+        // sm.part and sm.red are next written after the next item's masses,
+        // which every thread reaches only past the barrier above
     }
+}
+
+// the sample of each job after k_sample_ring: one CTA per job
+template <typename T>
+__global__ void __launch_bounds__(NT) k_sample_tail(const Params p)
+{
+    if (exit_skip(p)) return;
+    __shared__ SampleSmem sm;
+    const int jid = blockIdx.x;
+    const Job jb = load_job(p.jobs + jid);
+    if (jb.kind == JOB_NONE) return;
+    sample_tail<T>(p, jid, jb, make_job<T>(p, jb, jb.kind == JOB_RESIDUAL), sm);
 }
 
 // dense post-knob distribution of every valid draft row (draft-side sampler)
@@ -762,14 +771,20 @@ static cudaError_t launch_sample_ring(const Params& p, int njobs, cudaStream_t s
     const int64_t items = (int64_t)njobs * p.nseg_sample;
     const int grid = (int)std::min<int64_t>(items, (int64_t)g.sms * g.per_sm);
     k_sample_ring<T><<<grid, SR_THREADS, smem, s>>>(p, njobs);
+    cudaError_t e2 = cudaGetLastError();
+    if (e2 != cudaSuccess) return e2;
+    k_sample_tail<T><<<njobs, NT, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s)
+cudaError_t launch_sample(const Params& p, int dtype, int njobs, cudaStream_t s, int* launches)
 {
     if (njobs <= 0 || p.nseg_sample <= 0) return cudaSuccess;
-    if (rows_on_16(p, dtype))
+    if (rows_on_16(p, dtype)) {
+        if (launches) *launches += 2;
         return dtype == 1 ? launch_sample_ring<__nv_bfloat16>(p, njobs, s) : launch_sample_ring<float>(p, njobs, s);
+    }
+    if (launches) *launches += 1;
     // rows off 16 bytes: one CTA per (job, group of segments), about eight
     // CTAs per SM in all
     Params q = p;

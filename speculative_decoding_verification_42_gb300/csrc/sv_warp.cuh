@@ -22,6 +22,14 @@ struct __align__(16) WarpSmem {  // keys are written as 16-byte words
     int32_t qual[WM_CAND];
 };
 constexpr int WM_SMEM = WM_WARPS * (int)sizeof(WarpSmem);
+// a warp's share of the merge grid's shared memory: the whole WarpSmem for
+// chunk-key rows (the top-k gather stages candidates), its key staging alone
+// otherwise (histograms, the decision's lists), so that more rows fit an SM
+__host__ __device__ constexpr int wm_stride(int seg_mode)
+{
+    return seg_mode == SEG_CHUNK ? (int)sizeof(WarpSmem) : (int)sizeof(WarpSmem::keys);
+}
+static_assert(sizeof(WarpSmem::keys) % 16 == 0, "every warp's staging must start on 16 bytes");
 static_assert(sizeof(WarpSmem) % 16 == 0, "every warp's staging must start on 16 bytes");
 
 __device__ __forceinline__ void warp_bitonic_u64(unsigned long long* a, int n2)
@@ -748,6 +756,20 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
     return true;
 }
 
+// a non-negative float below 2^20 as a fixed-point integer in 2^-40 units,
+// rounded to nearest (zero, subnormals and anything below 2^-41 give 0)
+__device__ __forceinline__ unsigned long long to_fix40(float w)
+{
+    const uint32_t u = __float_as_uint(w);
+    const int ex = (int)(u >> 23);
+    if ((u >> 31) || ex == 0) return 0ull;
+    const unsigned long long m = (u & 0x7FFFFFu) | 0x800000u;  // w = m 2^(ex - 150)
+    const int sh = ex - 110;                                   // w 2^40 = m 2^sh
+    if (sh >= 0) return m << min(sh, 39);
+    if (sh < -24) return 0ull;
+    return (m + (1ull << (-sh - 1))) >> -sh;
+}
+
 // ------------------------------------------------------------------------- //
 // k_merge_warp: one warp per row slot (after the stream grid).  The last row //
 // of a sequence to finish (a ticket) decides the sequence.                   //
@@ -760,8 +782,9 @@ __device__ bool warp_decide(const Params& p, int b, unsigned char* stage)
 // token reaches top_p, ties at the cut key in ascending id (found in the one
 // segment holding the boundary token).  Fills st (MODE_PREFIX, P(x) at the
 // drafted token x) and returns true; false leaves the row to the block merge
-// (a saturated bin, the cut below the window, a nucleus of at most KCAP
-// tokens, which is kept as a list, or more than 32 segments).
+// (a saturated bin, the cut below the window, or more than 32 segments).  A
+// small nucleus stays a rank prefix too: its sample is drawn over the dense
+// row like any other, with the same masses a kept list would give.
 template <typename T>
 __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, WarpSmem& ws, RowStat& st)
 {
@@ -789,55 +812,83 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
     }
     __syncwarp();
     const uint32_t M16 = key16_bf16(__float_as_uint(M) >> 16);
+    // masses in fixed point (2^-40 units of the max token's): exact integer
+    // sums on the integer pipes, the per-key weights rounded once each
     // the tokens below each segment's own window (the stream's sums)
-    double below = (lane < nseg && ms > -INFINITY) ? ss * (double)exp2f((ms - M) * p.c) : 0.0;
-    // lane l holds the row's bins 8 l .. 8 l + 7 (bin d: key M16 - d)
-    uint32_t cnt[8];
+    unsigned long long below =
+        (lane < nseg && ms > -INFINITY) ? to_fix40((float)ss * exp2f((ms - M) * p.c)) : 0ull;
+    // lane l holds the row's bins 8 l .. 8 l + 7 (bin D: key M16 - D) and
+    // the bins 256 + 8 l .. below the window (weighed once per bin, not per
+    // segment); a segment whose window reaches below bin 511 weighs those
+    // bins itself (rare: its max lies over two binades below the row's)
+    uint32_t cnt[8], cntb[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) cnt[q] = 0u;
+    for (int q = 0; q < 8; ++q) cnt[q] = cntb[q] = 0u;
     bool sat = false;
     for (int i = 0; i < nseg; ++i) {
         const float mi = __shfl_sync(FULL, ms, i);
         if (!(mi > -INFINITY)) continue;
         const uint32_t m16 = key16_bf16(__float_as_uint(mi) >> 16);
-        const uint32_t off = M16 - m16;  // segment i's window starts off keys below the row's
+        const uint32_t off = M16 - m16;  // segment bin d is the row's bin off + d
         const uint8_t* Hi = H + i * HIST_BINS;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const uint32_t d = 8u * lane + q;
-            if (d >= off) {
-                const uint32_t c = Hi[d - off];
+            const uint32_t D = 8u * lane + q;
+            if (D >= off) {
+                const uint32_t c = Hi[D - off];
                 sat |= c == 255u;
                 cnt[q] += c;
             }
-            if (off + d >= (uint32_t)HIST_BINS) {  // segment bin d lies below the row's window
+            if (D + (uint32_t)HIST_BINS >= off && D + (uint32_t)HIST_BINS - off < (uint32_t)HIST_BINS) {
+                const uint32_t c = Hi[D + HIST_BINS - off];
+                sat |= c == 255u;
+                cntb[q] += c;
+            }
+        }
+        if (off > (uint32_t)HIST_BINS) {
+            // segment bins d with off + d >= 512
+            const uint32_t d0 = off >= 2u * HIST_BINS ? 0u : 2u * HIST_BINS - off;
+            for (uint32_t d = d0 + lane; d < (uint32_t)HIST_BINS; d += 32) {
                 const uint32_t c = Hi[d];
                 sat |= c == 255u;
-                if (c) below += (double)c * (double)hist_weight(p, m16 - d, M);
+                if (c) below += (unsigned long long)c * to_fix40(hist_weight(p, m16 - d, M));
             }
         }
     }
     if (__any_sync(FULL, sat)) return false;
-    double mass[8];
-    double lsum = 0.0;
+    unsigned long long mass[8], wq[8];
+    unsigned long long lsum = 0ull;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const uint32_t key = M16 - (8u * lane + q);
-        const float w = key >= 0x80u ? hist_weight(p, key, M) : 0.f;
-        mass[q] = (double)cnt[q] * (double)w;
+        wq[q] = key >= 0x80u ? to_fix40(hist_weight(p, key, M)) : 0ull;
+        mass[q] = (unsigned long long)cnt[q] * wq[q];
         lsum += mass[q];
+        const uint32_t keyb = key - HIST_BINS;
+        if (cntb[q] && key >= 0x80u + HIST_BINS)
+            below += (unsigned long long)cntb[q] * to_fix40(hist_weight(p, keyb, M));
     }
-    double incl = lsum;
+    unsigned long long incl = lsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(FULL, incl, o);
+        const unsigned long long y = __shfl_up_sync(FULL, incl, o);
         if (lane >= o) incl += y;
     }
-    const double S_all = __shfl_sync(FULL, incl, 31) + warp_sum_d(below);
-    const double target = (double)p.top_p * S_all;
+    unsigned long long bsum = below;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bsum += __shfl_xor_sync(FULL, bsum, o);
+    const unsigned long long S_all = __shfl_sync(FULL, incl, 31) + bsum;
+    // the strict rule: a token is kept while the mass before it is below
+    // top_p S; target = ceil(top_p S) in the same units (top_p_fix = top_p 2^56)
+    unsigned long long target;
+    {
+        const unsigned long long lo = p.top_p_fix * S_all, hi = __umul64hi(p.top_p_fix, S_all);
+        target = (hi << 8) | (lo >> 56);
+        if (lo & ((1ull << 56) - 1ull)) ++target;
+    }
     // the first bin whose inclusive mass reaches the target
     int cut = -1;
-    double above = 0.0, run = incl - lsum;
+    unsigned long long above = 0ull, run = incl - lsum;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         if (cut < 0 && cnt[q] > 0 && run < target && run + mass[q] >= target) {
@@ -852,19 +903,23 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
     cut = __shfl_sync(FULL, cut, src);
     above = __shfl_sync(FULL, above, src);
     int n_lane = 0, cntk = 0;
+    unsigned long long wk = 0ull;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const int d = 8 * lane + q;
         if (d < cut) n_lane += (int)cnt[q];
-        if (d == cut) cntk = (int)cnt[q];
+        if (d == cut) {
+            cntk = (int)cnt[q];
+            wk = wq[q];
+        }
     }
     const int n_above = __reduce_add_sync(FULL, n_lane);
     cntk = __reduce_add_sync(FULL, cntk);
+    wk = __shfl_sync(FULL, wk, src);
     const uint32_t kap16 = M16 - (uint32_t)cut;
-    const float wk = hist_weight(p, kap16, M);
-    int nk = (int)ceil((target - above) / (double)wk);
+    // the tokens of the cut key kept: the fewest whose mass reaches the target
+    int nk = (int)((target - above + wk - 1ull) / wk);
     nk = max(1, min(nk, cntk));
-    if (n_above + nk <= KCAP) return false;  // a list: the block merge builds it
     int32_t ik = p.V - 1;
     if (nk < cntk) {
         // the segment holding the nk-th token of key kap16 (in id order)
@@ -882,74 +937,54 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
         const unsigned hit = __ballot_sync(FULL, ci - cs < nk && nk <= ci);
         const int sseg = hit ? __ffs(hit) - 1 : 0;
         const int need = nk - __shfl_sync(FULL, ci - cs, sseg);  // 1-based among the segment's
-        // the segment in id order: lane l walks 256 contiguous tokens, 32
-        // 16-byte words loaded eight at a time
-        constexpr int PER = 256;
+        // the segment in id order, coalesced: round j holds words 32 j ..
+        // 32 j + 31 (lane l: word 32 j + l), eight rounds of loads in flight
         const unsigned short* rb = reinterpret_cast<const unsigned short*>(row);
-        const int e0 = sseg * (SEG_BYTES / 2) + lane * PER;
-        const int e_end = min(p.V, sseg * (SEG_BYTES / 2) + SEG_BYTES / 2);
-        // the lane's hits of key kap16, one 8-bit mask per word of the
-        // current group, counted per group of eight words
-        constexpr int NG = PER / 64;  // groups of eight words
-        auto group_hits = [&](int g, uint32_t (&hm)[8]) {
+        const int e_begin = sseg * (SEG_BYTES / 2);
+        const int nwd = (min(p.V, e_begin + SEG_BYTES / 2) - e_begin) / 8;  // whole words (V % 8 == 0)
+        int seen = 0, found = -1;
+        for (int j0 = 0; j0 * 32 < nwd && found < 0; j0 += 8) {
             uint4 v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int e = e0 + (8 * g + j) * 8;
-                v[j] = e < e_end ? __ldcg(reinterpret_cast<const uint4*>(rb + e)) : make_uint4(0, 0, 0, 0);
+                const int w = (j0 + j) * 32 + lane;
+                v[j] = w < nwd ? __ldcg(reinterpret_cast<const uint4*>(rb + e_begin + 8 * w)) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
+                const int w = (j0 + j) * 32 + lane;
                 const uint32_t xw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                hm[j] = 0u;
+                uint32_t hm = 0u;
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
-                    const int e = e0 + (8 * g + j) * 8 + h;
                     const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
-                    if (e < e_end && key16_bf16(b16) == kap16) hm[j] |= 1u << h;
+                    if (w < nwd && key16_bf16(b16) == kap16) hm |= 1u << h;
                 }
-            }
-        };
-        int gc[NG];
-        int mine = 0;
+                const int c = __popc(hm);
+                int in = c;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            uint32_t hm[8];
-            group_hits(g, hm);
-            gc[g] = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) gc[g] += __popc(hm[j]);
-            mine += gc[g];
-        }
-        int mi = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(FULL, mi, o);
-            if (lane >= o) mi += y;
-        }
-        int found = -1;
-        if (mi - mine < need && need <= mi) {
-            // the group holding it, re-read (one round from L2), then the word
-            int seen = mi - mine, g = 0;
-            while (g < NG - 1 && seen + gc[g] < need) seen += gc[g++];
-            uint32_t hm[8];
-            group_hits(g, hm);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (found < 0 && seen + __popc(hm[j]) >= need) {
-                    uint32_t m = hm[j];
-                    for (int q = 0; q < need - seen - 1; ++q) m &= m - 1u;  // drop the earlier hits
-                    found = e0 + (8 * g + j) * 8 + __ffs(m) - 1;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(FULL, in, o);
+                    if (lane >= o) in += y;
                 }
-                seen += __popc(hm[j]);
+                const int tot = __shfl_sync(FULL, in, 31);
+                if (found < 0 && seen + tot >= need) {
+                    int f = -1;
+                    if (seen + in - c < need && need <= seen + in) {
+                        uint32_t m = hm;
+                        for (int q = 0; q < need - (seen + in - c) - 1; ++q) m &= m - 1u;  // drop earlier hits
+                        f = e_begin + 8 * w + __ffs(m) - 1;
+                    }
+                    found = __reduce_max_sync(FULL, f);
+                }
+                seen += tot;
             }
         }
-        const unsigned f = __ballot_sync(FULL, found >= 0);
-        if (!f) return false;  // not found (cannot happen with exact counts): the block merge
-        ik = __shfl_sync(FULL, found, __ffs(f) - 1);
+        if (found < 0) return false;  // not found (cannot happen with exact counts): the block merge
+        ik = found;
     }
     st.M = M;
-    st.S = above + (double)nk * (double)wk;
+    st.S = (double)(above + (unsigned long long)nk * wk) * 0x1p-40;
     st.mode = MODE_PREFIX;
     st.kappa = key_of(val_key16(kap16));
     st.i_kappa = ik;
@@ -985,7 +1020,8 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
         return;
     }
     if (rr.is_draft && !drafts_streamed(p)) return;
-    WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_w)[warp];
+    // (only keys is touched outside chunk-key rows: see wm_stride)
+    WarpSmem& ws = *reinterpret_cast<WarpSmem*>(smem_w + (size_t)warp * wm_stride(p.seg_mode));
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     // the drafted token this row's P(x) is needed at (the bonus row has none)
     int x = -1;

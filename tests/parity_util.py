@@ -19,6 +19,14 @@ PROB_ATOL = 1e-9
 LSE_ATOL = 2e-5
 LSE_RTOL = 2.0 ** -22  # the output is fp32: two units in the last place at |lse|
 
+SUMMARY = []  # lines repeated in the session summary (conftest)
+
+
+def report(line: str):
+    """Print a result line now and again at the end of the session."""
+    print(line)
+    SUMMARY.append(line)
+
 
 def to_device(arr: np.ndarray):
     import torch

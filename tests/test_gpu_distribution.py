@@ -12,6 +12,8 @@ fp64 oracle's row softmax) must not reject at the pre-registered p = 1e-3."""
 import numpy as np
 import pytest
 
+from parity_util import report
+
 pytestmark = pytest.mark.gpu
 
 
@@ -64,5 +66,5 @@ def test_emitted_token_follows_target(orc, knobs):
     for counts, p in ((c0, p0), (c1, p1)):
         x, dof = _chisq(counts, p)
         pv = _chi2_sf(x, dof)
-        print(f"{knobs}: n = {counts.sum()}, chi2 = {x:.1f} on {dof} dof, p = {pv:.3g}")
+        report(f"{knobs}: n = {counts.sum()}, chi2 = {x:.1f} on {dof} dof, p = {pv:.3g}")
         assert pv > 1e-3, (knobs, x, dof, pv)

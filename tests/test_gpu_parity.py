@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from parity_util import (DELTA, compare, oracle_tokens, run_gpu, run_oracle, run_oracle_parallel,
-                         to_device)
+                         to_device, report)
 from workloads import make_config, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -38,7 +38,7 @@ def _check(orc, w, rows=None, max_near_frac=0.05, min_exact=None):
     idx = np.arange(w.B) if rows is None else np.asarray(rows)
     why = {k: int((o[k][idx] < DELTA).sum()) for k in ("margin_accept", "margin_topp",
                                                          "margin_cdf")}
-    print(f"{w.name}: {n - n_near} of {n} sequences compared bit-exactly; near-ties {why}")
+    report(f"{w.name}: {n - n_near} of {n} sequences compared bit-exactly; near-ties {why}")
     assert n_near <= max(1, max_near_frac * n), f"{n_near} near-tie rows of {n}: {why}"
     if min_exact is not None:
         assert n - n_near >= min_exact
@@ -296,7 +296,7 @@ def test_config3_full_size(orc):
     o = run_oracle_parallel(orc, w, toks)
     n_near = compare(g, o, w, toks)
     why = {k: int((o[k] < DELTA).sum()) for k in ("margin_accept", "margin_topp", "margin_cdf")}
-    print(f"{w.name}: {w.B - n_near} of {w.B} sequences bit-exact; near-ties {why}")
+    report(f"{w.name}: {w.B - n_near} of {w.B} sequences bit-exact; near-ties {why}")
     assert n_near <= max(1, 0.05 * w.B), why
 
 
@@ -343,7 +343,7 @@ def test_config4_full_size(orc):
             rel = np.abs(pg[live] / po[live] - 1.0)
             diff_margins += list(o[mname][b, :kb][live][rel > 1e-6])
     worst = max(diff_margins) if diff_margins else 0.0
-    print(f"{w.name}: {w.B - n_near} of {w.B} sequences bit-exact; near-ties {why}; "
+    report(f"{w.name}: {w.B - n_near} of {w.B} sequences bit-exact; near-ties {why}; "
           f"expected about {expect:.0f}; rows with another nucleus: {len(diff_margins)}, "
           f"largest oracle prefix margin among them {worst:.3g} (window {DELTA_TOPP_HIST:g})")
     assert worst < DELTA_TOPP_HIST, (worst, len(diff_margins))

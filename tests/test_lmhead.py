@@ -8,7 +8,7 @@ parity against the oracle verifying the same (GPU) logits."""
 import numpy as np
 import pytest
 
-from parity_util import DELTA, compare, run_oracle, run_oracle_parallel, to_device
+from parity_util import DELTA, compare, run_oracle, run_oracle_parallel, to_device, report
 
 pytestmark = pytest.mark.gpu
 
@@ -116,7 +116,7 @@ def test_fused_verify_config5_full(orc):
     o = run_oracle_parallel(orc, w5, toks)
     n_near = compare(gout, o, w5, toks)
     why = {k: int((o[k] < DELTA).sum()) for k in ("margin_accept", "margin_topp", "margin_cdf")}
-    print(f"fused round B={B}: {B - n_near} of {B} sequences bit-exact; near-ties {why}")
+    report(f"fused round B={B}: {B - n_near} of {B} sequences bit-exact; near-ties {why}")
     # without knobs the sample is an inverse CDF over all 128256 tokens, whose
     # masses are ~1e-5 of Z each: a CDF gap falls within 1e-6 Z of the target
     # in about a fifth of the sequences
