@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "verify rows/s (B·(K+1)) and achieved HBM GB/s vs GB300 peak, speculative sampling"
 UNIT = "rows/s"
 ROTATE = 3  # input copies cycled between steps (3 x 279 MB > L2)
+E2E_STREAMS = 4  # copy streams of the end-to-end measurement
 
 
 def _peaks():
@@ -60,19 +61,22 @@ def _stage1_kernel(w) -> str:
 
 
 def _traffic(kernel: str, w):
-    """DRAM bytes per launch of the kernel from the committed ncu capture, or
-    None when the capture is of another workload or of an older kernel."""
+    """DRAM bytes per launch of the kernel from the committed ncu capture of
+    this workload (one record, or a list of records, per kernel), or None when
+    there is none or it is of an older kernel source."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
-        e = d[kernel]
-        src = os.path.join(ROOT, "speculative_decoding_verification_42_gb300", "csrc", e["source"])
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if sha != e["source_sha256"] or e["workload"] != w.name:
-            return None
-        return float(e["dram_bytes_per_launch"])
+        recs = d[kernel]
+        for e in (recs if isinstance(recs, list) else [recs]):
+            if e["workload"] != w.name:
+                continue
+            src = os.path.join(ROOT, "speculative_decoding_verification_42_gb300", "csrc", e["source"])
+            with open(src, "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()
+            return float(e["dram_bytes_per_launch"]) if sha == e["source_sha256"] else None
+        return None
     except (OSError, KeyError, ValueError, TypeError):
         return None
 
@@ -578,8 +582,9 @@ def run_gpu(args):
     achieved = bytes_step / (ks["median_us"] * 1e-6) / 1e9
 
     # end to end: host buffers through the same call, copies inside the timed
-    # region; the inputs go in on two copy streams (target and draft on
-    # separate copy engines), the compute stream waits for both
+    # region; the inputs go in as E2E_STREAMS slices of each tensor on as many
+    # copy streams (several copy engines at once), the compute stream waits
+    # for all of them
     e2e = None
     if args.e2e_steps > 0:
         out = arm.out
@@ -595,32 +600,35 @@ def run_gpu(args):
         h_out_n = torch.empty(out["num_accepted"].shape, dtype=torch.int32, pin_memory=True)
         d_toks = torch.empty_like(toks)
         d_kpr = torch.empty_like(kpr)
-        cs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        cs = [torch.cuda.Stream(dev) for _ in range(E2E_STREAMS)]
         nrot = max(2, arm.n_rot)
         tgt = target if len(target) >= 2 else target * 2
         drf = draft if len(draft) >= 2 else draft * 2
-        ready = [torch.cuda.Event() for _ in range(2)]
+        ready = [torch.cuda.Event() for _ in range(E2E_STREAMS)]
         done = [torch.cuda.Event() for _ in range(nrot)]
 
-        def halves(t):
-            flat = t.view(-1)
-            n = flat.numel() // 2
-            return (flat[:n], flat[n:])
+        def slices(t):
+            flat = t.reshape(-1)
+            n = -(-flat.numel() // E2E_STREAMS)
+            return [flat[k * n:(k + 1) * n] for k in range(E2E_STREAMS)]
+
+        h_slices = list(zip(slices(h_target), slices(h_draft)))
+        d_slices = [list(zip(slices(tgt[c]), slices(drf[c]))) for c in range(nrot)]
 
         def e2e_step(i):
             c = i % nrot
             # the copies into buffer c wait for the step that last read it
-            for k, (dst, src) in enumerate(((tgt[c], h_target), (drf[c], h_draft))):
-                s = cs[k]
+            for k, s in enumerate(cs):
                 s.wait_event(done[c])
                 with torch.cuda.stream(s):
-                    dst.copy_(src, non_blocking=True)
+                    for dst, src in zip(d_slices[c][k], h_slices[k]):
+                        dst.copy_(src, non_blocking=True)
                     if k == 0:
                         d_toks.copy_(h_toks, non_blocking=True)
                         d_kpr.copy_(h_kpr, non_blocking=True)
                 ready[k].record(s)
-            stream.wait_event(ready[0])
-            stream.wait_event(ready[1])
+            for ev in ready:
+                stream.wait_event(ev)
             o = arm.ver.run(tgt[c], drf[c], d_toks, d_kpr, out=out, debug=False,
                             w_vocab=arm.wv, **arm.knobs)
             done[c].record(stream)
@@ -648,7 +656,8 @@ def run_gpu(args):
         e2e = {"value": whole_job_rate(rows, args.e2e_steps, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
-               "copies": "target and draft on two copy streams, double-buffered"}
+               "copies": f"target and draft in {E2E_STREAMS} slices each on {E2E_STREAMS} copy streams, "
+                         f"{nrot} device buffers"}
 
     fused = arm.fused
     verify_stage = _verify_stage(arm, 1e3 * mean_step_ms, ks["median_us"], peak) if fused else {}

@@ -215,12 +215,13 @@ spec_status spec_draft_sample(spec_verify_t h, const void* draft, const int32_t*
  *  - Sizes whose workspace would not fit the array return
  *    SPEC_ERR_INVALID_ARG and launch nothing.  The workspace is about
  *      per row slot (B * (2 K_max + 1) of them): 8244 bytes + 16 bytes per
- *        segment of 16 KB of the row + 2 bytes per 128-byte chunk of the row,
- *        i.e. 12.2 KiB at V = 128256 bf16 and 16.4 KiB at V = 128256 fp32;
+ *        segment of 16 KB of the row + 2 bytes per 128-byte chunk of the row
+ *        (but at least 256 bytes per 8192 tokens: the key histograms),
+ *        i.e. 12.3 KiB at V = 128256 bf16 and 16.4 KiB at V = 128256 fp32;
  *      per drafted slot (B * K_max of them): 28 bytes + 40 bytes per 4096
  *        tokens, i.e. 1.28 KiB at V = 128256;
  *    so B = 64 with K_max = 8 at V = 128256 bf16 (1088 row slots, 512
- *    drafted slots) needs 14.3 MB.
+ *    drafted slots) needs 14.4 MB.
  *  - Every call shares the one array and each call reuses the last call's
  *    contents (the counters that must start at zero are cleared on the
  *    stream first), so calls that overlap on the GPU race: issue them on one
