@@ -586,6 +586,23 @@ __device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+// polls that may sleep: the waiting thread is suspended for up to
+// MBAR_SLEEP_NS until the phase completes, so a warp that waits (a producer
+// for a free stage, a consumer for data) takes no issue slots from the
+// warps that compute; at most `limit` polls (0: WAIT_LIMIT / 64)
+constexpr uint32_t MBAR_SLEEP_NS = 2000;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit)
+{
+    const uint32_t n = limit ? limit : WAIT_LIMIT / 64;
+    for (uint32_t i = 0; i < n; ++i) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "n"(MBAR_SLEEP_NS) : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
 // one-dimensional bulk copy global -> shared, completing on an mbarrier
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
 {

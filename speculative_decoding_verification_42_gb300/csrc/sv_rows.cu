@@ -1695,12 +1695,20 @@ __device__ __forceinline__ float warp_hist_pos(const uint4* sv4, int nvalid, int
 {
     constexpr int SEGE = SEG_BYTES / 2;
     constexpr int WPL = SEGE / 8 / 32;
-    const float thrf = val_key16(lo16);
+    const uint32_t thr = __float_as_uint(val_key16(lo16)) >> 16;  // the window's lowest bf16
+    const uint32_t thr2 = thr | (thr << 16);
     const unsigned long long c2 = f2_pack(c, c), nmc2 = f2_pack(-Mc, -Mc);
     const uint32_t hb = smem_u32(hist) + 4u * (m16 - 0x8000u);  // hb - 4 h: the bin of bits h
+    // a token outside the window counts into the lane's own slot past the
+    // bins (never read): every lane issues every count, no branch
+    const uint32_t hdummy = smem_u32(hist) + 4u * (HIST_BINS + lane);
     unsigned long long s2[2] = {0ull, 0ull};  // four running sums, in two pairs
-    // (the counts need no memory clobber: the stage is only read here, and the
-    // warp's __syncwarp orders them before the histogram is read out)
+    // Per 32-bit word (two tokens): one packed bf16 compare gives both
+    // window predicates, one paired FMA both exponents (l c - M c), -inf
+    // where the token is counted instead, two ex2, one paired add, and the
+    // two shared-memory counts.  (No memory clobber: the stage is
+    // only read here, and the warp's __syncwarp orders the counts before the
+    // histogram is read out.)
 #pragma unroll 4
     for (int i = 0; i < WPL; ++i) {
         const int q = i * 32 + lane;
@@ -1708,18 +1716,35 @@ __device__ __forceinline__ float warp_hist_pos(const uint4* sv4, int nvalid, int
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            const uint32_t x = ws[h];
-            const float lo = bf16_lo(x), hi = bf16_hi(x);
-            const bool inlo = lo >= thrf, inhi = hi >= thrf;
-            float alo, ahi;
-            asm("mov.b64 {%0, %1}, %2;" : "=f"(alo), "=f"(ahi) : "l"(f2_fma(f2_pack(lo, hi), c2, nmc2)));
-            const float elo = ex2_fast(inlo ? -INFINITY : alo);
-            const float ehi = ex2_fast(inhi ? -INFINITY : ahi);
-            s2[h >> 1] = f2_add(s2[h >> 1], f2_pack(elo, ehi));
-            asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}"
-                         ::"r"(hb - ((x & 0xFFFFu) << 2)), "r"((uint32_t)inlo));
-            asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}"
-                         ::"r"(hb - ((x >> 16) << 2)), "r"((uint32_t)inhi));
+            asm volatile(
+                "{\n\t"
+                ".reg .pred plo, phi;\n\t"
+                ".reg .b32 blo, bhi, t;\n\t"
+                ".reg .f32 flo, fhi;\n\t"
+                ".reg .b64 a2;\n\t"
+                "setp.ge.bf16x2 plo|phi, %1, %2;\n\t"
+                "shl.b32 blo, %1, 16;\n\t"
+                "and.b32 bhi, %1, 0xFFFF0000;\n\t"
+                "mov.b64 a2, {blo, bhi};\n\t"
+                "fma.rn.f32x2 a2, a2, %3, %4;\n\t"
+                "mov.b64 {flo, fhi}, a2;\n\t"
+                "@plo mov.f32 flo, 0fFF800000;\n\t"
+                "@phi mov.f32 fhi, 0fFF800000;\n\t"
+                "ex2.approx.ftz.f32 flo, flo;\n\t"
+                "ex2.approx.ftz.f32 fhi, fhi;\n\t"
+                "mov.b64 a2, {flo, fhi};\n\t"
+                "add.rn.f32x2 %0, %0, a2;\n\t"
+                "and.b32 t, %1, 0xFFFF;\n\t"
+                "mad.lo.s32 t, t, -4, %5;\n\t"
+                "selp.b32 t, t, %6, plo;\n\t"
+                "red.shared.add.u32 [t], 1;\n\t"
+                "shr.u32 t, %1, 16;\n\t"
+                "mad.lo.s32 t, t, -4, %5;\n\t"
+                "selp.b32 t, t, %6, phi;\n\t"
+                "red.shared.add.u32 [t], 1;\n\t"
+                "}"
+                : "+l"(s2[h >> 1])
+                : "r"(ws[h]), "r"(thr2), "l"(c2), "l"(nmc2), "r"(hb), "r"(hdummy));
         }
     }
     return f2_sum(s2[0]) + f2_sum(s2[1]);
@@ -1827,11 +1852,12 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
     constexpr bool PERWARP = MODE != SEG_CHUNK;
     constexpr int NSENT = PERWARP ? NS / 32 : 1;  // end-of-work sentinels
     static_assert(!PERWARP || NSTAGE == NS / 32, "one stage per stream warp");
-    __shared__ uint32_t s_hist[MODE == SEG_HIST ? (NS / 32) * HIST_BINS : 1];
+    constexpr int HSTRIDE = HIST_BINS + 32;  // a warp's bins, then one spare count per lane
+    __shared__ uint32_t s_hist[MODE == SEG_HIST ? (NS / 32) * HSTRIDE : 1];
     using G = SegGeom<T, NS>;
     const int tid = threadIdx.x;
     if (MODE == SEG_HIST)
-        for (int i = tid; i < (NS / 32) * HIST_BINS; i += STREAM_THREADS) s_hist[i] = 0u;
+        for (int i = tid; i < (NS / 32) * HSTRIDE; i += STREAM_THREADS) s_hist[i] = 0u;
     // the merge kernel that follows may be scheduled as this grid drains; it
     // waits for this grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1863,7 +1889,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
                 if (rr.is_draft && !drafts_streamed(p)) continue;
             }
             const int s = k % NSTAGE;
-            if (k >= NSTAGE && !mbar_wait(&ring.empty[s], ((k / NSTAGE) - 1) & 1)) {
+            if (k >= NSTAGE && !mbar_wait_sleep(&ring.empty[s], ((k / NSTAGE) - 1) & 1, 0)) {
                 atomicOr(p.err, 1u);
                 failed = true;
                 break;
@@ -1875,7 +1901,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
                 for (int g = 1; g < NSENT; ++g) {
                     ++k;
                     const int s2 = k % NSTAGE;
-                    if (k >= NSTAGE && !mbar_wait(&ring.empty[s2], ((k / NSTAGE) - 1) & 1)) {
+                    if (k >= NSTAGE && !mbar_wait_sleep(&ring.empty[s2], ((k / NSTAGE) - 1) & 1, 0)) {
                         atomicOr(p.err, 1u);
                         break;
                     }
@@ -1908,7 +1934,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
         const int w = tid >> 5;
         for (int k = w;; k += NS / 32) {
             const int s = k % NSTAGE;
-            if (!__all_sync(FULL, mbar_wait_n(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
+            if (!__all_sync(FULL, mbar_wait_sleep(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
                 if ((tid & 31) == 0) atomicOr(p.err, 2u);
                 break;
             }
@@ -1916,7 +1942,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
             if (item < 0) break;
             const int r = item / p.nseg, seg = item - r * p.nseg;
             warp_segment<T, MODE>(p, reinterpret_cast<const uint4*>(smem_ring + (size_t)s * SEG_BYTES), seg, r,
-                                  s_hist + (MODE == SEG_HIST ? w * HIST_BINS : 0));
+                                  s_hist + (MODE == SEG_HIST ? w * HSTRIDE : 0));
             __syncwarp();  // every lane is done with the stage
             if ((tid & 31) == 0) mbar_arrive(&ring.empty[s]);
         }
@@ -1928,7 +1954,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 3) k_stream(const Params p)
         static_assert(PERWARP || MODE == SEG_CHUNK, "the shared-segment loop has no barriers");
         for (int k = 0;; ++k) {
             const int s = k % NSTAGE;
-            if (!__all_sync(0xffffffffu, mbar_wait_n(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(&ring.full[s], (k / NSTAGE) & 1, p.wait_limit))) {
                 if ((tid & 31) == 0) atomicOr(p.err, 2u);
                 break;
             }
