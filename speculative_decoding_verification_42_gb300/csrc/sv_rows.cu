@@ -43,12 +43,20 @@ template <typename T> struct Vec16;
 template <> struct Vec16<__nv_bfloat16> {
     static constexpr int N = 8;
     static __device__ __forceinline__ uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
-    static __device__ __forceinline__ float vmax(uint4 w)
+    // NaN-propagating max of two packed bf16 pairs, per half
+    static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b)
     {
-        float a = fmax_nan(fmax_nan(bf16_lo(w.x), bf16_hi(w.x)), fmax_nan(bf16_lo(w.y), bf16_hi(w.y)));
-        float b = fmax_nan(fmax_nan(bf16_lo(w.z), bf16_hi(w.z)), fmax_nan(bf16_lo(w.w), bf16_hi(w.w)));
-        return fmax_nan(a, b);
+        uint32_t r;
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+        return r;
     }
+    // the running packed max of a word's eight values (three paired maxima)
+    static __device__ __forceinline__ uint32_t vmax2(uint4 w, uint32_t acc)
+    {
+        return max2(acc, max2(max2(w.x, w.y), max2(w.z, w.w)));
+    }
+    static __device__ __forceinline__ float unpack_max(uint32_t m2) { return fmax_nan(bf16_lo(m2), bf16_hi(m2)); }
+    static __device__ __forceinline__ float vmax(uint4 w) { return unpack_max(max2(max2(w.x, w.y), max2(w.z, w.w))); }
     static __device__ __forceinline__ float vsumexp(uint4 w, float m, float c)
     {
         float s = 0.f;
@@ -1769,8 +1777,15 @@ __device__ __forceinline__ void warp_segment(const Params& p, const uint4* sv4, 
         return q * VW < nvalid ? sv4[q] : Vec16<T>::neg_inf();
     };
     float m = -INFINITY;
+    if constexpr (sizeof(T) == 2) {
+        uint32_t m2 = 0xFF80FF80u;  // -inf twice
 #pragma unroll 8
-    for (int i = 0; i < WPL; ++i) m = fmax_nan(m, Vec16<T>::vmax(word(i)));
+        for (int i = 0; i < WPL; ++i) m2 = Vec16<T>::vmax2(word(i), m2);
+        m = Vec16<T>::unpack_max(m2);
+    } else {
+#pragma unroll 8
+        for (int i = 0; i < WPL; ++i) m = fmax_nan(m, Vec16<T>::vmax(word(i)));
+    }
     const float M = warp_reduce_f(m, fmax_nan);
     float s = 0.f;
     if (M > -INFINITY && M < INFINITY) {
