@@ -377,6 +377,7 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
 // summing last segments (and drawing) for the rest of the grid.              //
 // ------------------------------------------------------------------------- //
 constexpr int SR_STAGES = 4;
+constexpr int SR_QUEUE = 64;  // kept tokens a warp weighs in one pass
 
 // bytes of one stage: the target segment, then the draft segment
 __host__ __device__ constexpr int sr_stage_bytes(int tsize, int dsize) { return SAMPLE_SEG * (tsize + dsize); }
@@ -452,6 +453,9 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
     __shared__ int s_item[SR_STAGES];
     __shared__ Job s_jb[SR_STAGES];
     __shared__ DenseJob s_job[SR_STAGES];
+    __shared__ int s_qv[NT / 32][SR_QUEUE];    // each warp's queue of kept tokens: id,
+    __shared__ float s_ql[NT / 32][SR_QUEUE];  // target logit
+    __shared__ float s_qd[NT / 32][SR_QUEUE];  // and draft value
     const int V = p.V, nseg = p.nseg_sample;
     const int dsize = p.draft_kind == 1 ? 4 : (int)sizeof(T);
     const int stage_bytes = sr_stage_bytes((int)sizeof(T), dsize);
@@ -558,13 +562,46 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
                     if (v0 + e < V) wm[q] += dense_r_fix(J, p.c, lt[e], dv[e], v0 + e, dptr);
             } else {
                 // R(v) = 0 wherever p_t(v) = 0 (outside the target's kept
-                // rank prefix): a mask of the word's kept tokens first, then
-                // the mass of those alone, in ascending v, so that a row with
-                // few kept tokens costs the warp a few passes, not one per token
+                // rank prefix): a mask of the word's kept tokens first
                 uint32_t km = 0u;
 #pragma unroll
                 for (int e = 0; e < G::SW; ++e)
                     if (v0 + e < V && kept_prefix(J.ts, key_of(lt[e]), v0 + e)) km |= 1u << e;
+                if (!(J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST)) {
+                    // the warp's kept tokens of this round go to the warp's
+                    // queue (in lane order) and are weighed one per lane, so a
+                    // row with few kept tokens costs the warp about one pass;
+                    // a lane keeps what overflows the queue
+                    const unsigned FULL = 0xffffffffu;
+                    const int cnt = __popc(km);
+                    int incl = cnt;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(FULL, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const int tot = __shfl_sync(FULL, incl, 31);
+                    int pos = incl - cnt;
+                    uint32_t own = 0u;  // kept tokens past the queue
+#pragma unroll
+                    for (int e = 0; e < G::SW; ++e) {
+                        if ((km >> e) & 1u) {
+                            if (pos < SR_QUEUE) {
+                                s_qv[warp][pos] = v0 + e;
+                                s_ql[warp][pos] = lt[e];
+                                s_qd[warp][pos] = dv[e];
+                            } else {
+                                own |= 1u << e;
+                            }
+                            ++pos;
+                        }
+                    }
+                    __syncwarp();
+                    for (int i = lane; i < min(tot, SR_QUEUE); i += 32)
+                        wm[q] += dense_r_fix(J, p.c, s_ql[warp][i], s_qd[warp][i], s_qv[warp][i], dptr);
+                    __syncwarp();  // the queue may be refilled
+                    km = own;
+                }
                 while (km) {
                     const int b = __ffs(km) - 1;
                     km &= km - 1u;
