@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
                 if (jb.kind == JOB_NONE) continue;
             }
             const int s = k % NST;
-            if (k >= NST && !mbar_wait(&s_empty[s], ((k / NST) - 1) & 1)) {
+            if (k >= NST && !mbar_wait_sleep(&s_empty[s], ((k / NST) - 1) & 1, 0)) {
                 atomicOr(p.err, 4u);
                 // wait (bounded) for the copies still in flight before leaving
                 for (int q = (k > NST ? k - NST : 0); q < k; ++q) mbar_wait(&s_full[q % NST], (q / NST) & 1);
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
     const int lane = tid & 31, warp = tid >> 5;
     for (int k = 0;; ++k) {
         const int s = k % NST;
-        if (!csync_and(mbar_wait_n(&s_full[s], (k / NST) & 1, p.wait_limit))) {
+        if (!csync_and(mbar_wait_sleep(&s_full[s], (k / NST) & 1, p.wait_limit))) {
             if (tid == 0) atomicOr(p.err, 4u);
             break;
         }
