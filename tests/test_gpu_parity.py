@@ -360,6 +360,45 @@ def test_ties_fall_back_and_keep_lowest_ids(orc):
     _check(orc, w)
 
 
+def _shift_bf16(w, delta):
+    """Every logit of a bf16 workload moved by delta (rounded back to bf16)."""
+    from workloads.synth import bf16_bits_to_f32, f32_to_bf16_bits
+    w.target = f32_to_bf16_bits(bf16_bits_to_f32(w.target) + np.float32(delta))
+    w.draft = f32_to_bf16_bits(bf16_bits_to_f32(w.draft) + np.float32(delta))
+    return w
+
+
+@pytest.mark.parametrize("case", ["negative", "all-equal", "flat", "over-32-segments"])
+def test_key_histogram_edges(orc, case):
+    """The nucleus of bf16 rows with top-p alone comes from per-segment key
+    histograms; each case takes a path the workloads do not:
+    negative: every logit below 0, so a segment's key window reaches zero and
+      the general (non-positive) counting loop runs;
+    all-equal: every token of a segment shares one key, the u8 bins saturate
+      and the block merge recomputes the row (ties keep the lowest ids);
+    flat: top-p 0.999 over N(0, 0.4^2) logits puts the cut more than 256 keys
+      below the max, outside the window: the radix descent finds it (each
+      token carries ~6e-5 of the mass, so a few rows are near-ties);
+    over-32-segments: V = 300000 has 37 segments, more than a warp stages, so
+      the block merge takes the histograms."""
+    if case == "negative":
+        w = _shift_bf16(make_workload(case, B=6, K_max=3, V=40000, dtype="bf16", target_std=2.0,
+                                      draft_noise_std=1.0, ragged_k=(0, 3), seed=41, top_p=0.9), -30.0)
+    elif case == "all-equal":
+        # (V = 19992: top_p V is far from an integer, so no prefix sits on top_p)
+        w = make_workload(case, B=4, K_max=2, V=19992, dtype="bf16", target_std=0.0,
+                          draft_noise_std=0.0, seed=43, top_p=0.9)
+    elif case == "flat":
+        w = make_workload(case, B=12, K_max=3, V=16384, dtype="bf16", target_std=0.4,
+                          draft_noise_std=0.2, ragged_k=(0, 3), seed=45, top_p=0.999)
+    else:
+        # (std 6: a nucleus of a few tokens, each carrying much of the mass,
+        # so no row of 300000 tokens sits within 1e-6 of top_p)
+        w = make_workload(case, B=4, K_max=2, V=300000, dtype="bf16", target_std=6.0,
+                          draft_noise_std=1.0, seed=47, top_p=0.9)
+    _check(orc, w, max_near_frac=0.34)
+
+
 def test_masked_and_invalid_rows(orc):
     import oracle as O
     w = make_workload("edge", B=10, K_max=3, V=3000, dtype="f32", ragged_k=(0, 3), seed=9,
