@@ -290,13 +290,25 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
                 }
                 uint32_t em[MCG_LPT];
                 int cnt = 0;
+                if constexpr (sizeof(T) == 2) {
+                    // bf16: a value reaches the bound iff its key does; one
+                    // packed compare per two values (-inf words never reach a
+                    // finite bound; a -inf bound admits them by key as well)
+                    const uint32_t thr2 = ChunkMax<T>::thr2(val_key16(tau_c));
 #pragma unroll
-                for (int j = 0; j < MCG_LPT; ++j) {
-                    em[j] = 0u;
+                    for (int j = 0; j < MCG_LPT; ++j) {
+                        em[j] = wi[j] >= 0 ? ChunkMax<T>::elem_mask(wv[j], 0.f, thr2) : 0u;
+                        cnt += __popc(em[j]);
+                    }
+                } else {
 #pragma unroll
-                    for (int q = 0; q < VW; ++q)
-                        if (wi[j] >= 0 && (key_of(word_elem_rt<T>(wv[j], q)) >> 16) >= tau_c) em[j] |= 1u << q;
-                    cnt += __popc(em[j]);
+                    for (int j = 0; j < MCG_LPT; ++j) {
+                        em[j] = 0u;
+#pragma unroll
+                        for (int q = 0; q < VW; ++q)
+                            if (wi[j] >= 0 && (key_of(word_elem_rt<T>(wv[j], q)) >> 16) >= tau_c) em[j] |= 1u << q;
+                        cnt += __popc(em[j]);
+                    }
                 }
                 int tot;
                 int pos = n + mc_excl_scan(cnt, sm.redi, &tot);
