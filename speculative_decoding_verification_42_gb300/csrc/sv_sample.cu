@@ -564,9 +564,29 @@ __global__ void __launch_bounds__(SR_THREADS, 3) k_sample_ring(const Params p, i
                 // R(v) = 0 wherever p_t(v) = 0 (outside the target's kept
                 // rank prefix): a mask of the word's kept tokens first
                 uint32_t km = 0u;
+                if (sizeof(T) == 2 && i + G::SW <= n) {
+                    // bf16: kept iff l > val(kappa), or l = val(kappa) at an id
+                    // <= i_kappa; packed compares, two values each
+                    const uint4 w = *reinterpret_cast<const uint4*>(st + (size_t)i * sizeof(T));
+                    const uint32_t kb = __float_as_uint(val_of(J.ts.kappa)) >> 16;
+                    const uint32_t k2u = kb | (kb << 16);
+                    const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(&k2u);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t gt = 0u, eq = 0u;
 #pragma unroll
-                for (int e = 0; e < G::SW; ++e)
-                    if (v0 + e < V && kept_prefix(J.ts, key_of(lt[e]), v0 + e)) km |= 1u << e;
+                    for (int h = 0; h < 4; ++h) {
+                        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&ws[h]);
+                        const uint32_t mg = __hgt2_mask(x, k2), me = __heq2_mask(x, k2);
+                        gt |= ((mg & 1u) | ((mg >> 15) & 2u)) << (2 * h);
+                        eq |= ((me & 1u) | ((me >> 15) & 2u)) << (2 * h);
+                    }
+                    const int ties_ok = min(max(J.ts.i_kappa - v0 + 1, 0), G::SW);  // ids v0 .. i_kappa
+                    km = gt | (eq & ((1u << ties_ok) - 1u));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < G::SW; ++e)
+                        if (v0 + e < V && kept_prefix(J.ts, key_of(lt[e]), v0 + e)) km |= 1u << e;
+                }
                 if (!(J.residual && J.dkind == 0 && J.ds.mode == MODE_LIST)) {
                     // the warp's kept tokens of this round go to the warp's
                     // queue (in lane order) and are weighed one per lane, so a
