@@ -295,16 +295,6 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(N
 
 // barrier of the stream warps of the streaming kernel (named barrier 2)
 __device__ __forceinline__ void ssync() { asm volatile("bar.sync 2, %0;" ::"n"(NS) : "memory"); }
-// the same barrier, returning whether v held in every stream thread (so that
-// a bounded wait that ran out in one thread ends the loop in all of them)
-__device__ __forceinline__ bool ssync_and(bool v)
-{
-    uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-                 "bar.red.and.pred p, 2, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(r) : "r"((uint32_t)v), "n"(NS) : "memory");
-    return r != 0;
-}
 
 // reductions over a thread group of NTH threads (local index lt) whose
 // barrier is SYNC(); red holds NTH/32 values
