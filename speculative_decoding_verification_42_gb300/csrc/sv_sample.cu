@@ -365,16 +365,18 @@ __global__ void __launch_bounds__(NT, 4) k_sample(const Params p)
 }
 
 // ------------------------------------------------------------------------- //
-// k_sample_ring: the same sums and sample for rows on 16 bytes, by a          //
-// persistent grid that streams the jobs' segments through shared memory.     //
-// Item i (job i / nseg, segment i % nseg) goes to CTA i mod gridDim; thread 0 //
-// keeps up to SR_STAGES items in flight as bulk copies (the target segment,  //
-// the draft segment when the residual reads the draft densely), each landing //
-// on the stage's mbarrier; every thread then sums its words of the stage in  //
-// the same fixed point and rounds as segment_pass.  The samples are drawn    //
-// by k_sample_tail, one CTA per job, after the whole grid: a CTA that drew   //
-// them as it summed a job's last segment fell behind the others and kept     //
-// summing last segments (and drawing) for the rest of the grid.              //
+// k_sample_ring: the same sums for rows on 16 bytes, by a persistent grid    //
+// that streams the jobs' segments through shared memory.  Item i (job       //
+// i / nseg, segment i % nseg) goes to CTA i mod gridDim.  The CTA's copy warp //
+// resolves each item's job and rows and keeps up to sr_stages() items in     //
+// flight as bulk copies (the target segment, and the draft segment when the  //
+// residual reads the draft densely), each landing on the stage's mbarrier;  //
+// the NT sampling threads then sum their words of the stage in the same     //
+// fixed point and rounds as segment_pass, weighing only the target's kept   //
+// tokens.  The samples are drawn by k_sample_tail, one CTA per job, after   //
+// the whole grid: a CTA that drew them as it summed a job's last segment    //
+// fell behind the others and kept summing last segments (and drawing) for   //
+// the rest of the grid.                                                      //
 // ------------------------------------------------------------------------- //
 constexpr int SR_STAGES = 4;
 constexpr int SR_QUEUE = 64;  // kept tokens a warp weighs in one pass
