@@ -61,6 +61,7 @@ def _run_noalloc(sv, torch, w, target, draft, toks, kpr, round_):
 @pytest.mark.parametrize("knobs,dtype,V", [
     (dict(top_k=50, temperature=0.8), "bf16", 32000),   # kept lists: decided in stage 1
     (dict(temperature=1.0), "f32", 20000),              # full rows: the stage-2 sampler
+    (dict(top_p=0.9), "bf16", 32768),                   # key histograms in the array, ring sampler
 ])
 def test_noalloc_equals_handle_entry_point_twice(orc, lib, knobs, dtype, V):
     import torch
