@@ -997,6 +997,57 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
     return true;
 }
 
+// The row slot of the g-th row the merge grid has work for, in sequence
+// order: each sequence's valid rows (target rows 0..K_b, then its draft rows
+// when they are streamed: seq_rows of them), or its slot 0 alone when K_b is
+// out of range (to report it); -1 past the last.  With a ragged batch the
+// valid rows then sit in the first warps of the grid, which fit the SMs at
+// once, instead of spreading over every slot of the batch's largest K.
+__device__ int warp_row_of(const Params& p, int g)
+{
+    const unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    constexpr int PER = 8;  // sequences a lane counts per round
+    int base = 0;           // rows of the sequences before this round's
+    for (int b0 = 0; b0 < p.B; b0 += 32 * PER) {
+        int cnt[PER], kbv[PER];
+        int mine = 0;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int b = b0 + lane * PER + e;
+            kbv[e] = b < p.B ? seq_k(p, b) : 0;
+            cnt[e] = b < p.B ? (k_ok(p, kbv[e]) ? seq_rows(p, kbv[e]) : 1) : 0;
+            mine += cnt[e];
+        }
+        int incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int tot = __shfl_sync(FULL, incl, 31);
+        if (g < base + tot) {
+            const int before = base + incl - mine;
+            int r = -1;
+            if (before <= g && g < before + mine) {
+                int i = g - before;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) {
+                    if (r < 0 && i < cnt[e]) {
+                        const int b = b0 + lane * PER + e, kb = kbv[e];
+                        const int slot = !k_ok(p, kb) ? 0 : (i <= kb ? i : p.Kmax + 1 + (i - kb - 1));
+                        r = b * p.rps + slot;
+                    }
+                    if (r < 0) i -= cnt[e];
+                }
+            }
+            return __reduce_max_sync(FULL, r);
+        }
+        base += tot;
+    }
+    return -1;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
 {
@@ -1007,8 +1058,13 @@ __global__ void __launch_bounds__(WM_WARPS * 32) k_merge_warp(const Params p)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const unsigned FULL = 0xffffffffu;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * WM_WARPS + warp;
-    if (r >= p.B * p.rps) return;
+    int r = blockIdx.x * WM_WARPS + warp;
+    if (p.kpr && !p.draft_launch) {
+        r = warp_row_of(p, r);  // per-row K: the valid rows first
+        if (r < 0) return;
+    } else if (r >= p.B * p.rps) {
+        return;
+    }
     // every load that does not depend on another goes out at once: the
     // sequence's K_b and the row's drafted token
     const int b = r / p.rps, slot = r - b * p.rps;
