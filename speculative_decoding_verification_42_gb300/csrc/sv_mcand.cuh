@@ -145,7 +145,6 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
     const T* row = (const T*)(rr.is_draft ? p.draft : p.target) + row_elem_offset(p, rr);
     const int x = (rr.j < rr.kb && x_raw >= 0 && x_raw < p.V) ? x_raw : -1;
     const int k = p.top_k;
-    if (tid == 0) sm.sel[2] = 0u;
 #pragma unroll
     for (int i = 0; i < MCG_BPT; ++i) sm.u.g.hist[i * MC_T + tid] = 0u;
 
@@ -174,10 +173,10 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
         for (int i = 0; i < 8; ++i)
             if (key_in(g, i)) tmax = max(tmax, key_at(g, i));
     const uint32_t wmax = __reduce_max_sync(FULL, tmax);
-    ssync();  // sel[2] and the histogram are cleared
-    if (lane == 0) atomicMax(&sm.sel[2], wmax);
-    ssync();
-    const uint32_t maxkey = sm.sel[2];
+    if (lane == 0) sm.redi[warp] = (int)wmax;
+    ssync();  // the warps' maxima are posted, the histogram is cleared
+    const uint32_t maxkey = max(max((uint32_t)sm.redi[0], (uint32_t)sm.redi[1]),
+                                max((uint32_t)sm.redi[2], (uint32_t)sm.redi[3]));
     if (maxkey >= 0xFF80u || maxkey <= 0x007Fu) {  // NaN or +inf, or no finite logit
         st.flags = FLAG_NONFINITE;
     } else {
@@ -194,8 +193,8 @@ __device__ RowStat merge_row_topk_core(const Params& p, int r, McSmem& sm)
             }
             int in_window;
             const int before = mc_excl_scan(local, sm.redi, &in_window);
-            if (tid == 0) sm.sel[3] = 0u;
-            ssync();
+            // (sel[3] is written by the thread holding the k-th key, read only
+            // when the window holds k keys: it needs no reset)
             if (before < k && before + local >= k) {
                 int run = before;
 #pragma unroll
