@@ -937,48 +937,78 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
         const unsigned hit = __ballot_sync(FULL, ci - cs < nk && nk <= ci);
         const int sseg = hit ? __ffs(hit) - 1 : 0;
         const int need = nk - __shfl_sync(FULL, ci - cs, sseg);  // 1-based among the segment's
-        // the segment in id order, coalesced: round j holds words 32 j ..
-        // 32 j + 31 (lane l: word 32 j + l), eight rounds of loads in flight
+        // the segment in batches of eight rounds of coalesced loads (round j
+        // of batch g: words 32 (8 g + j) .. + 31, lane l: word 32 (8 g + j)
+        // + l), from its end when the token lies in the later half of the
+        // segment's cs matches: the batch holding it is found from the
+        // batches' match counts alone, then the round and the lane in it
         const unsigned short* rb = reinterpret_cast<const unsigned short*>(row);
         const int e_begin = sseg * (SEG_BYTES / 2);
         const int nwd = (min(p.V, e_begin + SEG_BYTES / 2) - e_begin) / 8;  // whole words (V % 8 == 0)
-        int seen = 0, found = -1;
-        for (int j0 = 0; j0 * 32 < nwd && found < 0; j0 += 8) {
+        const int nbat = (nwd + 255) / 256;
+        const int csg = __shfl_sync(FULL, cs, sseg);  // the segment's tokens of key kap16
+        const bool back = 2 * need > csg + 1;
+        int want = back ? csg - need + 1 : need;  // 1-based, in the order the batches are read
+        int found = -1;
+        for (int i = 0; i < nbat; ++i) {
+            const int g = back ? nbat - 1 - i : i;
             uint4 v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int w = (j0 + j) * 32 + lane;
+                const int w = (8 * g + j) * 32 + lane;
                 v[j] = w < nwd ? __ldcg(reinterpret_cast<const uint4*>(rb + e_begin + 8 * w)) : make_uint4(0, 0, 0, 0);
             }
+            uint32_t hm[8];
+            int cl = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int w = (j0 + j) * 32 + lane;
+                const int w = (8 * g + j) * 32 + lane;
                 const uint32_t xw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                uint32_t hm = 0u;
+                hm[j] = 0u;
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
                     const uint32_t b16 = (h & 1) ? (xw[h >> 1] >> 16) : (xw[h >> 1] & 0xFFFFu);
-                    if (w < nwd && key16_bf16(b16) == kap16) hm |= 1u << h;
+                    if (w < nwd && key16_bf16(b16) == kap16) hm[j] |= 1u << h;
                 }
-                const int c = __popc(hm);
-                int in = c;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(FULL, in, o);
-                    if (lane >= o) in += y;
-                }
-                const int tot = __shfl_sync(FULL, in, 31);
-                if (found < 0 && seen + tot >= need) {
-                    int f = -1;
-                    if (seen + in - c < need && need <= seen + in) {
-                        uint32_t m = hm;
-                        for (int q = 0; q < need - (seen + in - c) - 1; ++q) m &= m - 1u;  // drop earlier hits
-                        f = e_begin + 8 * w + __ffs(m) - 1;
-                    }
-                    found = __reduce_max_sync(FULL, f);
-                }
-                seen += tot;
+                cl += __popc(hm[j]);
             }
+            const int tb = __reduce_add_sync(FULL, cl);
+            if (want > tb) {
+                want -= tb;
+                continue;
+            }
+            // this batch: the token is its need_b-th match in id order; the
+            // round holding it (warp-uniform), then the lane and the bit
+            int need_b = back ? tb - want + 1 : want;
+            int js = -1;
+            uint32_t mj = 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int tot = __reduce_add_sync(FULL, __popc(hm[j]));
+                if (js < 0) {
+                    if (need_b <= tot) {
+                        js = j;
+                        mj = hm[j];
+                    } else {
+                        need_b -= tot;
+                    }
+                }
+            }
+            const int c = __popc(mj);
+            int in = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL, in, o);
+                if (lane >= o) in += y;
+            }
+            int f = -1;
+            if (js >= 0 && in - c < need_b && need_b <= in) {
+                uint32_t m = mj;
+                for (int q = 0; q < need_b - (in - c) - 1; ++q) m &= m - 1u;  // drop earlier hits
+                f = e_begin + 8 * ((8 * g + js) * 32 + lane) + __ffs(m) - 1;
+            }
+            found = __reduce_max_sync(FULL, f);
+            break;
         }
         if (found < 0) return false;  // not found (cannot happen with exact counts): the block merge
         ik = found;
