@@ -821,41 +821,67 @@ __device__ bool warp_hist_nucleus(const Params& p, const T* row, int r, int x, W
     // the bins 256 + 8 l .. below the window (weighed once per bin, not per
     // segment); a segment whose window reaches below bin 511 weighs those
     // bins itself (rare: its max lies over two binades below the row's)
-    uint32_t cnt[8], cntb[8];
+    // per window (the bins 8 l .., then 256 + 8 l ..) four packed 16-bit
+    // sums of the lane's eight bins: bins 0 and 2, 1 and 3, 4 and 6, 5 and 7
+    // (at most 32 segments of at most 255 each: no carry between halves)
+    uint32_t acc[2][4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) cnt[q] = cntb[q] = 0u;
+    for (int k = 0; k < 4; ++k) acc[0][k] = acc[1][k] = 0u;
     bool sat = false;
     for (int i = 0; i < nseg; ++i) {
         const float mi = __shfl_sync(FULL, ms, i);
         if (!(mi > -INFINITY)) continue;
         const uint32_t m16 = key16_bf16(__float_as_uint(mi) >> 16);
         const uint32_t off = M16 - m16;  // segment bin d is the row's bin off + d
-        const uint8_t* Hi = H + i * HIST_BINS;
+        const uint8_t* Hb = H + i * HIST_BINS;
+        const uint32_t* Hi = reinterpret_cast<const uint32_t*>(Hb);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint32_t D = 8u * lane + q;
-            if (D >= off) {
-                const uint32_t c = Hi[D - off];
-                sat |= c == 255u;
-                cnt[q] += c;
-            }
-            if (D + (uint32_t)HIST_BINS >= off && D + (uint32_t)HIST_BINS - off < (uint32_t)HIST_BINS) {
-                const uint32_t c = Hi[D + HIST_BINS - off];
-                sat |= c == 255u;
-                cntb[q] += c;
-            }
+        for (int wd = 0; wd < 2; ++wd) {
+            // the lane's row bins 8 l + 256 wd + q are the segment's bins
+            // b + q, q < 8; those outside [0, HIST_BINS) count nothing.  The
+            // eight bytes from three words of the segment's histogram (word
+            // indices clamped to it: a clamped word only feeds bytes that
+            // the mask drops), shifted into place, then masked
+            const int b = 8 * lane + wd * HIST_BINS - (int)off;
+            if (b + 8 <= 0 || b >= HIST_BINS) continue;
+            const int w = b >> 2;  // floor: b may be negative
+            const uint32_t sh = (uint32_t)(b & 3) * 8u;
+            const uint32_t w0 = Hi[min(max(w, 0), HIST_BINS / 4 - 1)];
+            const uint32_t w1 = Hi[min(max(w + 1, 0), HIST_BINS / 4 - 1)];
+            const uint32_t w2 = Hi[min(max(w + 2, 0), HIST_BINS / 4 - 1)];
+            const int cut_lo = max(0, -b), cut_hi = max(0, b + 8 - HIST_BINS);
+            const unsigned long long keep = (~0ull << (8 * cut_lo)) & (~0ull >> (8 * cut_hi));
+            const uint32_t lo = __funnelshift_r(w0, w1, sh) & (uint32_t)keep;
+            const uint32_t hi = __funnelshift_r(w1, w2, sh) & (uint32_t)(keep >> 32);
+            // a saturated bin (255) among them: a zero byte in the complement
+            const uint32_t nl = ~lo, nh = ~hi;
+            sat |= ((((nl - 0x01010101u) & ~nl) | ((nh - 0x01010101u) & ~nh)) & 0x80808080u) != 0u;
+            acc[wd][0] += lo & 0x00FF00FFu;
+            acc[wd][1] += (lo >> 8) & 0x00FF00FFu;
+            acc[wd][2] += hi & 0x00FF00FFu;
+            acc[wd][3] += (hi >> 8) & 0x00FF00FFu;
         }
         if (off > (uint32_t)HIST_BINS) {
             // segment bins d with off + d >= 512
             const uint32_t d0 = off >= 2u * HIST_BINS ? 0u : 2u * HIST_BINS - off;
             for (uint32_t d = d0 + lane; d < (uint32_t)HIST_BINS; d += 32) {
-                const uint32_t c = Hi[d];
+                const uint32_t c = Hb[d];
                 sat |= c == 255u;
                 if (c) below += (unsigned long long)c * to_fix40(hist_weight(p, m16 - d, M));
             }
         }
     }
     if (__any_sync(FULL, sat)) return false;
+    uint32_t cnt[8], cntb[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        // sums k: bins (k & 1) + 4 (k >> 1) (low half) and that + 2 (high half)
+        const int q = (k & 1) + 4 * (k >> 1);
+        cnt[q] = acc[0][k] & 0xFFFFu;
+        cnt[q + 2] = acc[0][k] >> 16;
+        cntb[q] = acc[1][k] & 0xFFFFu;
+        cntb[q + 2] = acc[1][k] >> 16;
+    }
     unsigned long long mass[8], wq[8];
     unsigned long long lsum = 0ull;
 #pragma unroll
